@@ -1,0 +1,352 @@
+"""Throughput benchmark of the chunk-forward kkt_solve step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c5]
+
+One step = one kkt_solve over the whole workload ((2, 16384, 32, 128), bf16 keys,
+bf16 output by default) with inputs already resident in HBM.  The step's
+inputs and output (409 MB) exceed the 129 MB L2, so no flush is needed between
+steps.  Prints one JSON line (rank 0).  Under torchrun every rank runs the same
+workload on its own GPU (independent replicas: weak scaling, no data-path
+collective); timing is the max over ranks.
+
+--impl reference times the plain fp64 CPU oracle on the host cores instead (it
+is the only other implementation of this step that exists here), each step a
+bounded sample of tiles of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "token-heads/s and achieved HBM GB/s (% of GB300 peak) for kkt_solve, 1 GPU"
+UNIT = "token-heads/s"
+# Ascend 910B fused time for (2,16384,32,128) from the MindSpeed-Ops PR page's
+# performance table: 4.9368 ms -> 1,048,576 token-heads / 4.9368 ms.
+PAGE_FUSED_MS = {"c5": 4.9368}
+
+
+def bytes_per_token_head(wl, out_dtype: str) -> int:
+    """Algorithmic HBM bytes per token-head: read k (K bf16), g (fp32), beta
+    (bf16); write one output row of 64 values."""
+    b = wl.K * 2
+    b += 4 if wl.use_g else 0
+    b += 2 if wl.use_beta else 0
+    b += 64 * (2 if out_dtype == "bf16" else 4)
+    return b
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, path: str | None):
+        self.proc = None
+        self.path = path
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            f = open(self.path, "w") if self.path else subprocess.PIPE
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=f, stderr=subprocess.DEVNULL, text=True)
+            self._file = f if self.path else None
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        if self._file:
+            self._file.close()
+            out = open(self.path).read()
+        rows = [r.split(",") for r in (out or "").strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_reference(args, wl):
+    """Reference arm: the fp64 CPU oracle on a bounded sample of tiles per step."""
+    import oracle
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(wl)
+    threads = os.cpu_count() or 1
+    tiles = workloads.tile_list(wl)
+    rng = np.random.default_rng(2024)
+    # Calibrate the per-tile cost, then size each step so K steps take <= ~60 s.
+    calib = [tiles[i] for i in rng.choice(len(tiles), size=min(len(tiles), 4 * threads), replace=False)]
+    t0 = time.perf_counter()
+    oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], calib, threads=threads)
+    per_tile = (time.perf_counter() - t0) / len(calib)
+    per_step = max(1, min(len(tiles), int(60.0 / max(1, args.steps) / per_tile)))
+    samples = [[tiles[i] for i in rng.choice(len(tiles), size=per_step, replace=False)]
+               for _ in range(min(args.steps, 8))]
+    for w in range(args.warmup):
+        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], samples[w % len(samples)],
+                                   threads=threads)
+    th = 0
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        smp = samples[s % len(samples)]
+        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, threads=threads)
+        th += sum(t[4] for t in smp)
+    dt = time.perf_counter() - t0
+    value = th / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "K": wl.K, "chunk": 64,
+                   "impl": "plain C fp64 oracle, threads over tiles",
+                   "sample_tiles_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} random (chunk, head) tiles of {wl.name} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, inp, budget_s: float):
+    """The oracle, as it stands, on a bounded seeded sample of the workload."""
+    import oracle
+    threads = os.cpu_count() or 1
+    tiles = workloads.tile_list(wl)
+    rng = np.random.default_rng(7)
+    order = rng.permutation(len(tiles))
+    done, th, t0 = 0, 0, time.perf_counter()
+    batch = 8 * threads
+    while done < len(tiles) and time.perf_counter() - t0 < budget_s:
+        smp = [tiles[i] for i in order[done:done + batch]]
+        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, threads=threads)
+        done += len(smp)
+        th += sum(t[4] for t in smp)
+    dt = time.perf_counter() - t0
+    return {"value": th / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} random (chunk, head) tiles of {wl.name} ({th} token-heads) in {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c5", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--out-dtype", default=None, choices=["f32", "bf16"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    wl = workloads.CONFIGS[args.config]
+    out_dtype = args.out_dtype or wl.out_dtype
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import gated_deltanet_chunked_gdr_gb300 as gdr
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+
+    inp = workloads.make_inputs(wl)
+    k = inp["k"].to(dev)
+    g = None if inp["g"] is None else inp["g"].to(dev)
+    beta = None if inp["beta"] is None else inp["beta"].to(dev)
+    cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].to(dev)
+    odt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    out = torch.empty((*k.shape[:3], 64), dtype=odt, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+    B = cu.numel() - 1 if cu is not None else k.shape[0]
+
+    def step(o=out):
+        rc = gdr.kkt_solve_raw(k.data_ptr(), 0 if g is None else g.data_ptr(),
+                               0 if beta is None else beta.data_ptr(),
+                               0 if cu is None else cu.data_ptr(), B, k.shape[1], wl.H, wl.K, 64,
+                               gdr.GDR_BF16 if out_dtype == "bf16" else gdr.GDR_F32,
+                               o.data_ptr(), sh)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_kkt_solve")
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if gdr.device_status() != gdr.GDR_OK:
+        raise RuntimeError("device status not ok after warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    gpu_id = ("GPU-" + gpu_id) if gpu_id and not gpu_id.startswith("GPU-") else (gpu_id or str(local))
+    sampler = ClockSampler(gpu_id, args.clocks_csv if rank == 0 else None)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)                                  # let the sampler start
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    th_rank = wl.token_heads
+    value = ws * th_rank / (ms_step * 1e-3)
+    if gdr.device_status() != gdr.GDR_OK:
+        raise RuntimeError("device status not ok after the timed region")
+
+    # End to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the call, D2H of the full output.
+    hk = inp["k"].pin_memory()
+    hg = None if inp["g"] is None else inp["g"].pin_memory()
+    hb = None if inp["beta"] is None else inp["beta"].pin_memory()
+    hcu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].pin_memory()
+    hout = torch.empty(out.shape, dtype=odt).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hg, hb, hcu) if t is not None)
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dk = hk.to(dev, non_blocking=True)
+            dg = None if hg is None else hg.to(dev, non_blocking=True)
+            db = None if hb is None else hb.to(dev, non_blocking=True)
+            dc = None if hcu is None else hcu.to(dev, non_blocking=True)
+            o = gdr.kkt_solve(dk, dg, db, dc, output_dtype=odt, stream=sh)
+            hout.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    barrier()
+
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        bpt = bytes_per_token_head(wl, out_dtype)
+        achieved = th_rank * bpt / (ms_step * 1e-3) / 1e9
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tpath):
+            with open(tpath) as f:
+                tj = json.load(f)
+            key = f"{wl.name}:{out_dtype}"
+            if key in tj:
+                traffic = tj[key]
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": (value / (th_rank / (PAGE_FUSED_MS[args.config] * 1e-3))
+                            if args.config in PAGE_FUSED_MS else None),
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "K": wl.K,
+                       "chunk": 64, "k": "bf16", "g": "f32", "beta": "bf16", "out": out_dtype,
+                       "compute": "Gram bf16xbf16->f32 (tcgen05), gate/solve f32",
+                       "l2": f"no flush: inputs+output {th_rank * bpt / 1e6:.0f} MB/step > 129 MB L2",
+                       "parallelism": f"replicas x{ws} (independent tiles, no collective)",
+                       "vs_baseline_ref": "Ascend 910B fused Triton time from the PR page table"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                         "bytes_per_token_head": bpt},
+            "e2e": {"value": ws * th_rank / (e2e_ms * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

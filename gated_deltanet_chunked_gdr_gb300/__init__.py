@@ -1,0 +1,159 @@
+"""GB300 (sm_103a) chunk-forward kkt_solve of Gated DeltaNet.
+
+Thin Python binding over the C ABI declared in include/gdr_kkt_solve.h.  This
+module only marshals arguments (pointers, sizes, the current CUDA stream);
+every step of the computation runs in the CUDA library.  There is no CPU
+fallback: if the library is missing or no sm_103 GPU is present, calls raise.
+
+Python signature mirrors the API of the MindSpeed-Ops PR #135 page ("feat(triton):
+add chunk_gated_delta_rule_fwd_kkt_solve", API block):
+    kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size=64, output_dtype=None)
+    -> (I + A)^{-1} as [B, T, H, 64]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+GDR_OK = 0
+GDR_ERR_NULL = -1
+GDR_ERR_SHAPE = -2
+GDR_ERR_CHUNK = -3
+GDR_ERR_DTYPE = -4
+GDR_ERR_ALIGN = -5
+GDR_ERR_DEVICE = -6
+GDR_ERR_CUDA = -7
+GDR_ERR_TIMEOUT = -8
+GDR_F32 = 0
+GDR_BF16 = 1
+
+EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_status_string", "gdr_kkt_solve_device_status",
+                    "gdr_kkt_solve_num_sms")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GdrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load the compiled library (building it first if the sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _build.needs_build():
+                _build.build()
+            lib = ctypes.CDLL(_build.LIB_PATH)
+            vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            lib.gdr_kkt_solve.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp, vp]
+            lib.gdr_kkt_solve.restype = ci
+            lib.gdr_status_string.argtypes = [ci]
+            lib.gdr_status_string.restype = ctypes.c_char_p
+            lib.gdr_kkt_solve_device_status.argtypes = [ctypes.POINTER(ci)]
+            lib.gdr_kkt_solve_device_status.restype = ci
+            lib.gdr_kkt_solve_num_sms.argtypes = []
+            lib.gdr_kkt_solve_num_sms.restype = ci
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().gdr_status_string(int(status)).decode()
+
+
+def kkt_solve_raw(k_ptr: int, g_ptr: int, beta_ptr: int, cu_ptr: int, B: int, T: int, H: int,
+                  K: int, chunk_size: int, out_dtype: int, out_ptr: int, stream: int) -> int:
+    """Direct C-ABI call with integer pointers; returns the gdr_status code."""
+    return load_library().gdr_kkt_solve(k_ptr or None, g_ptr or None, beta_ptr or None,
+                                        cu_ptr or None, B, T, H, K, chunk_size, out_dtype,
+                                        out_ptr or None, stream or None)
+
+
+def device_status() -> int:
+    """Reads and clears the device-side status word (synchronises the device)."""
+    v = ctypes.c_int(0)
+    rc = load_library().gdr_kkt_solve_device_status(ctypes.byref(v))
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_kkt_solve_device_status")
+    return v.value
+
+
+def num_sms() -> int:
+    rc = load_library().gdr_kkt_solve_num_sms()
+    if rc < 0:
+        raise GdrError(rc, "gdr_kkt_solve_num_sms")
+    return rc
+
+
+def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, output_dtype=None,
+              out=None, stream=None):
+    """(I + A)^{-1} of every 64-token chunk and head, on the GPU.
+
+    k: bf16 [B, T, H, 128] CUDA tensor ([1, T, H, 128] with cu_seqlens);
+    g: fp32 [B, T, H] or None; beta: bf16 [B, T, H] or None;
+    cu_seqlens: int32 [N + 1] CUDA tensor or None; output_dtype: torch.float32
+    (default) or torch.bfloat16.  Returns out [B, T, H, 64]."""
+    import torch
+
+    if chunk_size != 64:
+        raise ValueError("chunk_size must be 64")
+    if output_dtype is None:
+        output_dtype = torch.float32
+    if output_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("output_dtype must be torch.float32 or torch.bfloat16")
+    if k.dtype != torch.bfloat16 or k.dim() != 4 or not k.is_cuda:
+        raise TypeError("k must be a 4-D bf16 CUDA tensor")
+    for name, t, dt in (("g", g, torch.float32), ("beta", beta, torch.bfloat16),
+                        ("cu_seqlens", cu_seqlens, torch.int32)):
+        if t is not None and (t.dtype != dt or t.device != k.device):
+            raise TypeError(f"{name} must be a {dt} tensor on {k.device}")
+    Bk, T, H, K = k.shape
+    if cu_seqlens is not None:
+        if Bk != 1 or cu_seqlens.dim() != 1:
+            raise ValueError("with cu_seqlens, k must be [1, T, H, K] and cu_seqlens 1-D")
+        B = cu_seqlens.numel() - 1
+    else:
+        B = Bk
+    for name, t in (("g", g), ("beta", beta)):
+        if t is not None and tuple(t.shape) != (Bk, T, H):
+            raise ValueError(f"{name} must have shape {(Bk, T, H)}")
+    k = k.contiguous()
+    g = None if g is None else g.contiguous()
+    beta = None if beta is None else beta.contiguous()
+    cu_seqlens = None if cu_seqlens is None else cu_seqlens.contiguous()
+    if out is None:
+        out = torch.empty((Bk, T, H, 64), dtype=output_dtype, device=k.device)
+    elif out.dtype != output_dtype or tuple(out.shape) != (Bk, T, H, 64) or not out.is_contiguous():
+        raise ValueError("out has the wrong dtype, shape or layout")
+    if stream is None:
+        stream = torch.cuda.current_stream(k.device).cuda_stream
+    with torch.cuda.device(k.device):
+        rc = kkt_solve_raw(k.data_ptr(), 0 if g is None else g.data_ptr(),
+                           0 if beta is None else beta.data_ptr(),
+                           0 if cu_seqlens is None else cu_seqlens.data_ptr(),
+                           B, T, H, K, chunk_size,
+                           GDR_BF16 if output_dtype == torch.bfloat16 else GDR_F32,
+                           out.data_ptr(), int(stream))
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_kkt_solve")
+    return out
+
+
+__all__ = ["kkt_solve", "kkt_solve_raw", "device_status", "num_sms", "build", "load_library",
+           "status_string", "GdrError", "EXPORTED_SYMBOLS"]

@@ -1,0 +1,766 @@
+// gdr_kkt_solve.cu - GB300 (sm_103a) fused chunk-forward kkt_solve of Gated DeltaNet.
+//
+// Computes, for every 64-token chunk and head, X = (I + A)^{-1} with
+//   A[i][j] = beta_i * (k_i . k_j) * exp(g_i - g_j)   (j < i < L), 0 otherwise,
+// and writes X as out[B, T, H, 64] (MindSpeed-Ops PR #135 page, "feat(triton): add
+// chunk_gated_delta_rule_fwd_kkt_solve", section "What this PR does": one call
+// replaces solve_tril(chunk_scaled_dot_kkt_fwd(...)); API block: result
+// (I+A)^{-1} of shape [B, T, H, 64]).  The intermediate A never leaves the SM
+// and no separate zero-fill pass runs.
+//
+// Kernel organisation (one persistent CTA per SM, 14 warps):
+//   warp 12      producer: walks the tile schedule and TMA-loads the key tiles of
+//                two (chunk, head) tiles per pipeline stage (bf16, 128-byte swizzle).
+//   warp 13      MMA issuer: allocates TMEM and, per stage, issues tcgen05.mma
+//                (kind::f16, M=128 = both tiles' 64 rows, N=64 = one tile's rows,
+//                K=128) twice, so TMEM holds K0*K0^T and K1*K1^T in fp32.
+//   warps 0..11  three consumer warpgroups; each owns 128 TMEM columns and one
+//                tile pair at a time:
+//                  epilogue - each thread reads its row of S = K*K^T from TMEM,
+//                             applies beta_i, exp(g_i - g_j) (exponent clamped to
+//                             [-50, 50] as in the page's bot summary) and writes
+//                             row i of A to shared memory;
+//                  solve    - each lane owns one output row c and runs a
+//                             right-looking substitution for row c of (I+A)^{-1}
+//                             in fp32 registers; warps take the 16-row blocks of
+//                             the chunk (the page's 16x16 sub-blocks BC=16) in a
+//                             rotating order so the triangular work spreads evenly;
+//                  store    - rows are staged in shared memory and written with
+//                             coalesced 128-bit stores (rows past the chunk end are
+//                             not written, zero columns are written explicitly).
+// Every mbarrier wait is bounded by wall time; on expiry the kernel records
+// GDR_ERR_TIMEOUT in a device status word and all roles leave their loops.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+#include <stdint.h>
+
+#include "gdr_kkt_solve.h"
+
+namespace gdr {
+
+constexpr int kChunk = 64;
+constexpr int kHeadK = 128;
+constexpr int kNumWG = 3;
+constexpr int kNumStages = 3;
+constexpr int kNumConsumerWarps = 4 * kNumWG;
+constexpr int kProducerWarp = kNumConsumerWarps;
+constexpr int kMmaWarp = kNumConsumerWarps + 1;
+constexpr int kNumThreads = (kNumConsumerWarps + 2) * 32;
+
+constexpr int kBoxBytes = kChunk * 64 * 2;          // one (tile, K-half) box: 64 rows x 128 B
+constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][128 B] = 32 KB
+constexpr int kAPitch = 68;                         // floats per A row (68*4 = 272 B)
+constexpr int kATileBytes = kChunk * kAPitch * 4;   // 17408
+constexpr int kATile1Off = kATileBytes + 16;        // second tile shifted by 16 B (other banks)
+constexpr int kAWGBytes = 34944;                    // >= kATile1Off + kATileBytes, multiple of 128
+constexpr int kGWGBytes = 2 * 2 * kChunk * 4;       // g of two tiles, double buffered
+constexpr uint32_t kTmemCols = 512;
+
+constexpr int kOffK = 0;
+constexpr int kOffA = kOffK + kNumStages * kStageBytes;
+constexpr int kOffG = kOffA + kNumWG * kAWGBytes;
+constexpr int kOffBar = kOffG + kNumWG * kGWGBytes;
+constexpr int kNumBars = 2 * kNumStages + 2 * kNumWG;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemUsed = kOffMisc + 64;
+constexpr int kSmemBytes = kSmemUsed + 1024;        // slack for 1024-byte alignment
+
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffA % 1024 == 0, "stages must keep 1024-byte alignment");
+
+constexpr uint64_t kWaitNs = 2000000000ull;         // 2 s bound for every wait
+
+struct Params {
+    const float *g;
+    const __nv_bfloat16 *beta;
+    const int32_t *cu;
+    void *out;
+    int64_t B, T, H;
+    int64_t n_slots;   // chunk slots: fixed-length B*NT, varlen floor((T + 63 B)/64)
+    int64_t NT;        // chunks per sequence (fixed-length)
+    int64_t n_pairs;   // ceil(n_slots * H / 2)
+    int *status;
+};
+
+struct Tile {
+    int64_t row0;      // first token row of the chunk in the flattened token axis
+    int L;             // rows in the chunk; 0 = no tile
+    int h;
+};
+
+__device__ int g_status_word = 0;
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for the phase with the given parity to complete; false after kWaitNs.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer() - t0 > kWaitNs) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Ties registers written by tcgen05.ld to a point after tcgen05.wait::ld, so the
+// compiler cannot hoist their first use above the wait.
+__device__ __forceinline__ void reg_fence(uint32_t &r) { asm volatile("" : "+r"(r)); }
+
+// Shared-memory matrix descriptor of a K-major bf16 operand stored as 8-row x
+// 128-byte swizzle atoms (the layout a 128-byte-swizzled TMA box produces):
+// start address, leading offset (unused for this layout), stride between 8-row
+// groups = 1024 B, descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N=64, M=128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) |
+                            ((128u >> 4) << 24);
+
+// ------------------------------------------------------------ tile schedule
+// Tile u = slot * H + h.  Fixed-length: slot = b * NT + c.  Varlen: sequence n
+// owns the slots [base(n), base(n+1)) with base(n) = floor((cu[n] + 63 n) / 64),
+// which leaves room for its ceil(len/64) chunks (at most one slot stays empty).
+__device__ __forceinline__ Tile tile_of(const Params &p, int64_t u) {
+    Tile t;
+    t.row0 = 0;
+    t.L = 0;
+    t.h = static_cast<int>(u % p.H);
+    const int64_t slot = u / p.H;
+    if (slot >= p.n_slots) return t;
+    if (p.cu == nullptr) {
+        const int64_t b = slot / p.NT;
+        const int64_t c = slot - b * p.NT;
+        t.row0 = b * p.T + c * kChunk;
+        const int64_t rem = p.T - c * kChunk;
+        t.L = static_cast<int>(rem < kChunk ? rem : kChunk);
+        return t;
+    }
+    int64_t lo = 0, hi = p.B;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        const int64_t bm = (static_cast<int64_t>(__ldg(p.cu + mid)) + 63 * mid) >> 6;
+        if (bm <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    if (lo >= p.B) return t;
+    const int64_t s = __ldg(p.cu + lo);
+    int64_t e = __ldg(p.cu + lo + 1);
+    if (e > p.T) e = p.T;
+    const int64_t c = slot - ((s + 63 * lo) >> 6);
+    const int64_t r0 = s + c * kChunk;
+    if (c < 0 || s < 0 || r0 >= e) return t;
+    t.row0 = r0;
+    t.L = static_cast<int>(e - r0 < kChunk ? e - r0 : kChunk);
+    return t;
+}
+
+// ---------------------------------------------------------------- the solve
+// Right-looking substitution for row c of (I + A)^{-1}.  y[j] accumulates
+// -sum_{i>j} A[i][j] * y[i]; processing i from the top down, y[i] becomes final
+// (plus 1 on the diagonal) and is pushed into every y[j], j < i.  Rows i above
+// c give y[i] = 0, so one instruction stream serves all 16 rows of a block.
+template <int TOP>
+__device__ __forceinline__ void solve_rows(float (&y)[64], const float *A, int c) {
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+        const int i = TOP - ii;
+        y[i] += (i == c) ? 1.0f : 0.0f;
+        const float yi = y[i];
+        const float4 *Ar = reinterpret_cast<const float4 *>(A + i * kAPitch);
+#pragma unroll
+        for (int j4 = 0; j4 < (i + 3) / 4; ++j4) {
+            const float4 a = Ar[j4];
+            if (4 * j4 + 0 < i) y[4 * j4 + 0] = fmaf(-a.x, yi, y[4 * j4 + 0]);
+            if (4 * j4 + 1 < i) y[4 * j4 + 1] = fmaf(-a.y, yi, y[4 * j4 + 1]);
+            if (4 * j4 + 2 < i) y[4 * j4 + 2] = fmaf(-a.z, yi, y[4 * j4 + 2]);
+            if (4 * j4 + 3 < i) y[4 * j4 + 3] = fmaf(-a.w, yi, y[4 * j4 + 3]);
+        }
+    }
+}
+
+__device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag) {
+    *abort_flag = 1;
+    atomicExch(p.status, static_cast<int>(GDR_ERR_TIMEOUT));
+}
+
+__device__ __forceinline__ Tile pick(const Tile &a, const Tile &b, bool second) {
+    Tile t;
+    t.row0 = second ? b.row0 : a.row0;
+    t.L = second ? b.L : a.L;
+    t.h = second ? b.h : a.h;
+    return t;
+}
+
+__device__ __forceinline__ void load_gb(const Params &p, const Tile &t, int i, float &gv,
+                                        float &bv) {
+    gv = 0.0f;
+    bv = 0.0f;
+    if (i < t.L) {
+        const int64_t idx = (t.row0 + i) * p.H + t.h;
+        gv = p.g ? __ldg(p.g + idx) : 0.0f;
+        bv = p.beta ? __bfloat162float(p.beta[idx]) : 1.0f;
+    }
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + kOffBar;                       // [kNumStages]
+    const uint32_t bar_empty = bar_full + 8 * kNumStages;            // [kNumStages]
+    const uint32_t bar_tfull = bar_empty + 8 * kNumStages;           // [kNumWG]
+    const uint32_t bar_tempty = bar_tfull + 8 * kNumWG;              // [kNumWG]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    volatile int *wg_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);   // [kNumWG]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNumStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int w = 0; w < kNumWG; ++w) {
+            mbar_init(bar_tfull + 8 * w, 1);
+            mbar_init(bar_tempty + 8 * w, 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int64_t n_local = (p.n_pairs > blockIdx.x)
+                                ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
+                                : 0;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
+                         : "memory");
+            int64_t q = 0;
+            for (; q < n_local; ++q) {
+                if (*abort_flag) break;
+                const int s = static_cast<int>(q % kNumStages);
+                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
+                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+                    record_timeout(p, abort_flag);
+                    break;
+                }
+                const int64_t pair = blockIdx.x + q * gridDim.x;
+                const Tile t0 = tile_of(p, 2 * pair);
+                const Tile t1 = tile_of(p, 2 * pair + 1);
+                const uint32_t bytes = (t0.L > 0 ? 2 * kBoxBytes : 0) + (t1.L > 0 ? 2 * kBoxBytes : 0);
+                const uint32_t st = sbase + kOffK + s * kStageBytes;
+                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+                if (t0.L > 0) {
+                    tma_load_3d(st + 0 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t0.h,
+                                static_cast<int>(t0.row0));
+                    tma_load_3d(st + 2 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t0.h,
+                                static_cast<int>(t0.row0));
+                }
+                if (t1.L > 0) {
+                    tma_load_3d(st + 1 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t1.h,
+                                static_cast<int>(t1.row0));
+                    tma_load_3d(st + 3 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t1.h,
+                                static_cast<int>(t1.row0));
+                }
+            }
+            // Drain: every issued load has landed and every stage's MMAs committed.
+            const int64_t first = q > kNumStages ? q - kNumStages : 0;
+            for (int64_t r = first; r < q; ++r) {
+                const int s = static_cast<int>(r % kNumStages);
+                const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
+                if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
+                if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            int64_t q = 0;
+            for (; q < n_local; ++q) {
+                if (*abort_flag) break;
+                const int s = static_cast<int>(q % kNumStages);
+                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
+                const int w = static_cast<int>(q % kNumWG);
+                const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
+                if (!mbar_wait(bar_full + 8 * s, ph) || !mbar_wait(bar_tempty + 8 * w, phw ^ 1)) {
+                    record_timeout(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = sbase + kOffK + s * kStageBytes;
+#pragma unroll
+                for (int bt = 0; bt < 2; ++bt) {
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
+#pragma unroll
+                    for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
+                            const uint32_t b_addr = a_addr + bt * kBoxBytes;
+                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(b_addr), kIdesc,
+                                       (kh | ks) ? 1u : 0u);
+                        }
+                    }
+                }
+                tc_commit(bar_empty + 8 * s);
+                tc_commit(bar_tfull + 8 * w);
+            }
+            // The last pair's MMAs must be complete before TMEM is released.
+            if (q > 0) {
+                const int64_t r = q - 1;
+                const int w = static_cast<int>(r % kNumWG);
+                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
+                    record_timeout(p, abort_flag);
+            }
+        }
+    } else {
+        // ------------------------------------------------ consumer warpgroups
+        const int wg = warp >> 2;
+        const int qd = warp & 3;                 // TMEM lane quadrant of this warp
+        const int tt_e = qd >> 1;                // epilogue: tile of this thread's row
+        const int i_e = 32 * (qd & 1) + lane;    // epilogue: row within the tile
+        uint8_t *abuf = smem + kOffA + wg * kAWGBytes;
+        float *gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);
+        const int bar_id = 1 + wg;
+
+        int64_t q = wg;
+        Tile cur0 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x));
+        Tile cur1 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x) + 1);
+        float gv, bv;
+        load_gb(p, pick(cur0, cur1, tt_e), i_e, gv, bv);
+
+        for (int r = 0; q < n_local; ++r, q += kNumWG) {
+            // Prefetch the next pair's schedule and g/beta.
+            const int64_t qn = q + kNumWG;
+            Tile nx0, nx1;
+            nx0.L = nx1.L = 0;
+            nx0.row0 = nx1.row0 = 0;
+            nx0.h = nx1.h = 0;
+            if (qn < n_local) {
+                nx0 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x));
+                nx1 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x) + 1);
+            }
+            float gn, bn;
+            load_gb(p, pick(nx0, nx1, tt_e), i_e, gn, bn);
+
+            if (qd == 0 && lane == 0) {
+                int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
+                if (!ok) record_timeout(p, abort_flag);
+                wg_flag[wg] = ok;
+            }
+            float *gcur = gbuf + (r & 1) * 2 * kChunk;
+            gcur[tt_e * kChunk + i_e] = gv;
+            named_bar_sync(bar_id, 128);                       // B2: g ready, A free
+            if (!wg_flag[wg]) break;
+            tc_fence_after();
+
+            // ---- epilogue: S row from TMEM -> A row in shared memory
+            {
+                uint32_t sr[64];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
+                                       static_cast<uint32_t>(128 * wg + 64 * tt_e);
+                {
+                    uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
+                    uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
+                    tmem_ld32(taddr, lo);
+                    tmem_ld32(taddr + 32, hi);
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 64; ++j) reg_fence(sr[j]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
+
+                const Tile te = pick(cur0, cur1, tt_e);
+                float *Arow = reinterpret_cast<float *>(abuf + (tt_e ? kATile1Off : 0)) +
+                              i_e * kAPitch;
+                const float *gt = gcur + tt_e * kChunk;
+                if (i_e < te.L) {
+                    const float gi = gv;
+                    const float bi = bv;
+                    if ((qd & 1) == 0) {
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 gj = *reinterpret_cast<const float4 *>(gt + 4 * j4);
+                            float4 a;
+                            a.x = bi * __uint_as_float(sr[4 * j4 + 0]) *
+                                  __expf(fminf(fmaxf(gi - gj.x, -50.f), 50.f));
+                            a.y = bi * __uint_as_float(sr[4 * j4 + 1]) *
+                                  __expf(fminf(fmaxf(gi - gj.y, -50.f), 50.f));
+                            a.z = bi * __uint_as_float(sr[4 * j4 + 2]) *
+                                  __expf(fminf(fmaxf(gi - gj.z, -50.f), 50.f));
+                            a.w = bi * __uint_as_float(sr[4 * j4 + 3]) *
+                                  __expf(fminf(fmaxf(gi - gj.w, -50.f), 50.f));
+                            reinterpret_cast<float4 *>(Arow)[j4] = a;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j4 = 0; j4 < 16; ++j4) {
+                            const float4 gj = *reinterpret_cast<const float4 *>(gt + 4 * j4);
+                            float4 a;
+                            a.x = bi * __uint_as_float(sr[4 * j4 + 0]) *
+                                  __expf(fminf(fmaxf(gi - gj.x, -50.f), 50.f));
+                            a.y = bi * __uint_as_float(sr[4 * j4 + 1]) *
+                                  __expf(fminf(fmaxf(gi - gj.y, -50.f), 50.f));
+                            a.z = bi * __uint_as_float(sr[4 * j4 + 2]) *
+                                  __expf(fminf(fmaxf(gi - gj.z, -50.f), 50.f));
+                            a.w = bi * __uint_as_float(sr[4 * j4 + 3]) *
+                                  __expf(fminf(fmaxf(gi - gj.w, -50.f), 50.f));
+                            reinterpret_cast<float4 *>(Arow)[j4] = a;
+                        }
+                    }
+                } else {
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int j4 = 0; j4 < 16; ++j4) reinterpret_cast<float4 *>(Arow)[j4] = z;
+                }
+            }
+            named_bar_sync(bar_id, 128);                       // B3: A complete
+
+            // ---- solve: lane -> (tile, row c) of block s
+            const int sblk = (qd + r) & 3;
+            const int tt = lane >> 4;
+            const int c = 16 * sblk + (lane & 15);
+            const float *A = reinterpret_cast<const float *>(abuf + (tt ? kATile1Off : 0));
+            float y[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) y[j] = 0.0f;
+            if (sblk == 3) solve_rows<63>(y, A, c);
+            if (sblk >= 2) solve_rows<47>(y, A, c);
+            if (sblk >= 1) solve_rows<31>(y, A, c);
+            solve_rows<15>(y, A, c);
+            named_bar_sync(bar_id, 128);                       // B4: A no longer read
+
+            // ---- store: stage own rows in the A buffer, then coalesced 16-B stores
+            {
+                uint8_t *rowp = abuf + (tt ? kATile1Off : 0) + c * (kAPitch * 4);
+                if (OUT_BF16) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        uint4 v;
+                        __nv_bfloat162 b0 = __floats2bfloat162_rn(y[8 * q4 + 0], y[8 * q4 + 1]);
+                        __nv_bfloat162 b1 = __floats2bfloat162_rn(y[8 * q4 + 2], y[8 * q4 + 3]);
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(y[8 * q4 + 4], y[8 * q4 + 5]);
+                        __nv_bfloat162 b3 = __floats2bfloat162_rn(y[8 * q4 + 6], y[8 * q4 + 7]);
+                        v.x = *reinterpret_cast<uint32_t *>(&b0);
+                        v.y = *reinterpret_cast<uint32_t *>(&b1);
+                        v.z = *reinterpret_cast<uint32_t *>(&b2);
+                        v.w = *reinterpret_cast<uint32_t *>(&b3);
+                        reinterpret_cast<uint4 *>(rowp)[q4] = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < 16; ++q4)
+                        reinterpret_cast<float4 *>(rowp)[q4] =
+                            make_float4(y[4 * q4 + 0], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
+                }
+                __syncwarp();
+                constexpr int kChunksPerRow = OUT_BF16 ? 8 : 16;      // 16-byte pieces per row
+                constexpr int kRowsPerIter = 32 / kChunksPerRow;
+#pragma unroll
+                for (int it = 0; it < 32 / kRowsPerIter; ++it) {
+                    const int rho = it * kRowsPerIter + lane / kChunksPerRow;   // 0..31
+                    const int piece = lane % kChunksPerRow;
+                    const int tts = rho >> 4;
+                    const int cs = 16 * sblk + (rho & 15);
+                    const Tile ts = pick(cur0, cur1, tts);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        abuf + (tts ? kATile1Off : 0) + cs * (kAPitch * 4) + 16 * piece);
+                    if (cs < ts.L) {
+                        const int64_t row = (ts.row0 + cs) * p.H + ts.h;
+                        uint8_t *dst = reinterpret_cast<uint8_t *>(p.out) +
+                                       row * (OUT_BF16 ? 128 : 256) + 16 * piece;
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                    }
+                }
+            }
+            cur0 = nx0;
+            cur1 = nx1;
+            gv = gn;
+            bv = bn;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_ready[kMaxDevices];   // 0 unknown, 1 ready, -1 unsupported
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+int prepare_device(int *sms) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GDR_ERR_DEVICE;
+    }
+    int st = g_dev_ready[dev].load(std::memory_order_acquire);
+    if (st == 0) {
+        int major = 0, minor = 0, nsm = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GDR_ERR_DEVICE;
+        }
+        if (major != 10 || minor != 3) {
+            g_dev_ready[dev].store(-1, std::memory_order_release);
+            return GDR_ERR_DEVICE;
+        }
+        if (cudaFuncSetAttribute(kkt_solve_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(kkt_solve_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GDR_ERR_CUDA;
+        }
+        g_dev_sms[dev].store(nsm, std::memory_order_relaxed);
+        g_dev_ready[dev].store(1, std::memory_order_release);
+        st = 1;
+    }
+    if (st < 0) return GDR_ERR_DEVICE;
+    *sms = g_dev_sms[dev].load(std::memory_order_relaxed);
+    return GDR_OK;
+}
+
+}  // namespace gdr
+
+extern "C" {
+
+const char *gdr_status_string(int status) {
+    switch (status) {
+        case GDR_OK: return "ok";
+        case GDR_ERR_NULL: return "a required pointer is NULL";
+        case GDR_ERR_SHAPE: return "unsupported or inconsistent sizes (K must be 128; B*T < 2^31)";
+        case GDR_ERR_CHUNK: return "chunk_size must be 64";
+        case GDR_ERR_DTYPE: return "out_dtype must be GDR_F32 or GDR_BF16";
+        case GDR_ERR_ALIGN: return "pointer misaligned (k and out 16 B, g 4 B, beta 2 B, cu_seqlens 4 B)";
+        case GDR_ERR_DEVICE: return "no usable CUDA device (an sm_103 GPU is required)";
+        case GDR_ERR_CUDA: return "a CUDA runtime or driver call failed";
+        case GDR_ERR_TIMEOUT: return "a device-side pipeline wait timed out";
+        default: return "unknown gdr_status";
+    }
+}
+
+int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t *cu_seqlens,
+                  int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size, int out_dtype,
+                  void *out, void *stream) {
+    using namespace gdr;
+    if (chunk_size != kChunk) return GDR_ERR_CHUNK;
+    if (out_dtype != GDR_F32 && out_dtype != GDR_BF16) return GDR_ERR_DTYPE;
+    if (B < 0 || T < 0 || H < 0 || K != kHeadK) return GDR_ERR_SHAPE;
+    if (B == 0 || T == 0 || H == 0) return GDR_OK;
+    if (!k || !out) return GDR_ERR_NULL;
+    const int64_t ntok = cu_seqlens ? T : B * T;
+    if (B > (int64_t(1) << 31) || T > (int64_t(1) << 31) || ntok >= (int64_t(1) << 31) ||
+        H > (int64_t(1) << 24) || (cu_seqlens == nullptr && B > ((int64_t(1) << 31) / T)))
+        return GDR_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
+        (reinterpret_cast<uintptr_t>(g) & 3) || (reinterpret_cast<uintptr_t>(beta) & 1) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens) & 3))
+        return GDR_ERR_ALIGN;
+
+    int sms = 0;
+    int rc = prepare_device(&sms);
+    if (rc != GDR_OK) return rc;
+    auto encode = encode_fn();
+    if (!encode) return GDR_ERR_CUDA;
+
+    CUtensorMap tmap;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(ntok)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K * 2),
+                                   static_cast<cuuint64_t>(H * K * 2)};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kChunk)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return GDR_ERR_CUDA;
+
+    Params prm;
+    prm.g = g;
+    prm.beta = static_cast<const __nv_bfloat16 *>(beta);
+    prm.cu = cu_seqlens;
+    prm.out = out;
+    prm.B = B;
+    prm.T = T;
+    prm.H = H;
+    prm.NT = (T + kChunk - 1) / kChunk;
+    prm.n_slots = cu_seqlens ? (T + 63 * B) / kChunk : B * prm.NT;
+    prm.n_pairs = (prm.n_slots * H + 1) / 2;
+    int *status_ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status_ptr), g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        return GDR_ERR_CUDA;
+    }
+    prm.status = status_ptr;
+
+    const int64_t grid = prm.n_pairs < sms ? prm.n_pairs : sms;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (out_dtype == GDR_BF16)
+        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
+    else
+        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
+    if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
+int gdr_kkt_solve_device_status(int *status) {
+    if (!status) return GDR_ERR_NULL;
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&v, gdr::g_status_word, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return GDR_ERR_CUDA;
+    }
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(gdr::g_status_word, &zero, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return GDR_ERR_CUDA;
+    }
+    *status = v;
+    return GDR_OK;
+}
+
+int gdr_kkt_solve_num_sms(void) {
+    int sms = 0;
+    int rc = gdr::prepare_device(&sms);
+    return rc == GDR_OK ? sms : rc;
+}
+
+}  // extern "C"

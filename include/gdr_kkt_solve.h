@@ -1,0 +1,107 @@
+/*
+ * gdr_kkt_solve.h - C ABI of the GB300 (sm_103a) chunk-forward kkt_solve step of
+ * Gated DeltaNet.
+ *
+ * Operation (MindSpeed-Ops PR #135 page, "feat(triton): add
+ * chunk_gated_delta_rule_fwd_kkt_solve", section "What this PR does" and its
+ * API block): one call equals solve_tril(chunk_scaled_dot_kkt_fwd(k, g, beta)).
+ * For every sequence, every chunk of at most 64 tokens counted from the
+ * sequence start, and every head h:
+ *     A[i][j] = beta_i * (k_i . k_j) * exp(g_i - g_j)   for j < i < L, else 0
+ *     out[chunk row i][h][0..63] = row i of (I + A)^{-1}
+ * with L <= 64 the chunk's length.  Columns >= L of a partial chunk are 0.  The
+ * gate exponent is clamped to [-50, 50] as on the same page's bot summary; for
+ * chunk-local log-decays (g non-increasing inside a chunk) the clamp never binds
+ * on the lower triangle.
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  Nothing is
+ *     allocated or freed by the library, and nothing is retained after return.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream) and the call returns without synchronising.
+ *   - Errors are returned as gdr_status codes; the library never aborts, traps
+ *     or prints.  Argument errors are detected on the host before any launch,
+ *     and then nothing is enqueued and `out` is untouched.
+ *   - Calls are thread-safe (no mutable host state besides a once-initialised
+ *     driver entry point).
+ */
+#ifndef GDR_KKT_SOLVE_H
+#define GDR_KKT_SOLVE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDR_OK = 0,
+    GDR_ERR_NULL = -1,    /* a required pointer is NULL                        */
+    GDR_ERR_SHAPE = -2,   /* negative size, unsupported K, or size overflow    */
+    GDR_ERR_CHUNK = -3,   /* chunk_size != 64                                  */
+    GDR_ERR_DTYPE = -4,   /* out_dtype is not a gdr_dtype value                */
+    GDR_ERR_ALIGN = -5,   /* a pointer is not aligned as documented below      */
+    GDR_ERR_DEVICE = -6,  /* no current CUDA device, or it is not sm_103       */
+    GDR_ERR_CUDA = -7,    /* a CUDA runtime/driver call failed (launch, TMA map) */
+    GDR_ERR_TIMEOUT = -8  /* a device-side bounded wait ran out (see gdr_kkt_solve_device_status) */
+} gdr_status;
+
+typedef enum {
+    GDR_F32 = 0,          /* IEEE fp32 output                                 */
+    GDR_BF16 = 1          /* bfloat16 output, round-to-nearest-even from fp32 */
+} gdr_dtype;
+
+/*
+ * gdr_kkt_solve - (I + A)^{-1} of every 64-token chunk and head.
+ *
+ *   k          bf16 [B, T, H, K] contiguous; with cu_seqlens: [1, T, H, K].
+ *              16-byte aligned.  K must be 128.
+ *   g          fp32 [B, T, H] (same leading layout as k) chunk-local cumulative
+ *              log-gate, or NULL (gate factor 1).  4-byte aligned.
+ *   beta       bf16 [B, T, H], or NULL (beta = 1).  2-byte aligned.
+ *   cu_seqlens int32 [B + 1] device array, or NULL.  When given, B is the number
+ *              of packed sequences, T the total token count, and sequence n
+ *              covers token rows [cu[n], cu[n+1]); chunks restart at every
+ *              sequence start (same page, bot summary: the T_local fix).  The
+ *              contents are the caller's contract: cu[0] = 0, non-decreasing,
+ *              cu[B] <= T.  Token rows outside every sequence are not written.
+ *   B, T, H, K sizes; B, T or H equal to 0 is an empty problem (returns GDR_OK,
+ *              enqueues nothing).  B*T must be below 2^31.
+ *   chunk_size must be 64 (GDR_ERR_CHUNK otherwise, like the page's API, which
+ *              raises ValueError for other chunk sizes).
+ *   out_dtype  GDR_F32 or GDR_BF16.
+ *   out        [B, T, H, 64] of out_dtype, 16-byte aligned.  Every row of a
+ *              real token is fully written (zeros included); no separate
+ *              zero-fill is needed.  Must not overlap the inputs.
+ *   stream     cudaStream_t as void*.
+ * Returns GDR_OK when the kernel was enqueued, else an error code.
+ */
+int gdr_kkt_solve(const void *k, const float *g, const void *beta,
+                  const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
+                  int64_t K, int chunk_size, int out_dtype, void *out,
+                  void *stream);
+
+/* Human-readable text for a gdr_status value (static storage, never NULL). */
+const char *gdr_status_string(int status);
+
+/*
+ * gdr_kkt_solve_device_status - reads the device-side status word of the
+ * current device and resets it to GDR_OK.  Synchronises the current device.
+ * The kernel's pipeline waits are bounded; if one ever runs out (a defect, not
+ * an input error), the kernel stops early, leaves its outputs incomplete and
+ * records GDR_ERR_TIMEOUT here.  Writes the recorded status to *status and
+ * returns GDR_OK, or GDR_ERR_NULL / GDR_ERR_CUDA.
+ */
+int gdr_kkt_solve_device_status(int *status);
+
+/*
+ * gdr_kkt_solve_num_sms - number of persistent CTAs one call launches at most
+ * on the current device (one per SM).  Returns a negative gdr_status on error.
+ */
+int gdr_kkt_solve_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_KKT_SOLVE_H */

@@ -1,0 +1,112 @@
+"""Host-only tests of the C-ABI boundary: the library loads, exports every entry
+point its header declares, and rejects bad arguments with the documented codes
+before touching the GPU.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_chunked_gdr_gb300 as gdr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(gdr_[A-Za-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    lib = gdr.load_library()
+    declared = _declared_functions()
+    assert {"gdr_kkt_solve", "gdr_status_string"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared <= set(gdr.EXPORTED_SYMBOLS)
+
+
+def test_status_strings():
+    for code in range(-8, 1):
+        s = gdr.status_string(code)
+        assert isinstance(s, str) and s and s != "unknown gdr_status"
+    assert gdr.status_string(-99) == "unknown gdr_status"
+
+
+# Fake, well-aligned addresses: validation must fail before anything uses them.
+K_PTR, OUT_PTR, G_PTR, B_PTR, CU_PTR = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+
+
+def _call(**kw):
+    a = dict(k=K_PTR, g=G_PTR, beta=B_PTR, cu=0, B=2, T=100, H=3, K=128, chunk=64,
+             dtype=gdr.GDR_F32, out=OUT_PTR)
+    a.update(kw)
+    return gdr.kkt_solve_raw(a["k"], a["g"], a["beta"], a["cu"], a["B"], a["T"], a["H"], a["K"],
+                             a["chunk"], a["dtype"], a["out"], 0)
+
+
+@pytest.mark.parametrize("chunk", [0, 16, 32, 63, 65, 128])
+def test_chunk_size_must_be_64(chunk):
+    assert _call(chunk=chunk) == gdr.GDR_ERR_CHUNK
+
+
+@pytest.mark.parametrize("dtype", [-1, 2, 7])
+def test_bad_out_dtype(dtype):
+    assert _call(dtype=dtype) == gdr.GDR_ERR_DTYPE
+
+
+@pytest.mark.parametrize("kw", [dict(K=64), dict(K=256), dict(K=127), dict(B=-1), dict(T=-5),
+                                dict(H=-2), dict(B=1 << 20, T=1 << 12),
+                                dict(cu=CU_PTR, B=4, T=1 << 31)])
+def test_bad_shapes(kw):
+    assert _call(**kw) == gdr.GDR_ERR_SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(T=0), dict(H=0), dict(B=0, k=0, out=0)])
+def test_empty_problem_is_ok_and_launches_nothing(kw):
+    assert _call(**kw) == gdr.GDR_OK
+
+
+@pytest.mark.parametrize("kw", [dict(k=0), dict(out=0)])
+def test_null_pointers(kw):
+    assert _call(**kw) == gdr.GDR_ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(k=K_PTR + 8), dict(out=OUT_PTR + 4), dict(g=G_PTR + 2),
+                                dict(beta=B_PTR + 1), dict(cu=CU_PTR + 2)])
+def test_misaligned_pointers(kw):
+    assert _call(**kw) == gdr.GDR_ERR_ALIGN
+
+
+def test_valid_arguments_without_gpu_report_device_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this test covers the no-device path")
+    assert _call() == gdr.GDR_ERR_DEVICE
+    assert gdr.load_library().gdr_kkt_solve_num_sms() == gdr.GDR_ERR_DEVICE
+
+
+def test_python_binding_rejects_chunk_size_like_the_page_api():
+    import torch
+    k = torch.zeros(1, 64, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gdr.kkt_solve(k, chunk_size=32)
+    with pytest.raises(TypeError):
+        gdr.kkt_solve(k)                       # CPU tensor: no CPU fallback exists
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "gated_deltanet_chunked_gdr_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "oracle_kkt_solve" not in text, fn

@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances (fixed for the method): fp32 output max_abs <= 2e-3 and
+mean_rel <= 1e-5; bf16 output max_abs <= 1.5e-2, with
+max_abs = max |gpu - ref| and mean_rel = sum |gpu - ref| / sum |ref| over the
+rows of real tokens.  Small workloads are compared element by element in full;
+the (2, 16384, 32, 128) workload is compared on a seeded sample of tiles
+(including every partial chunk) and checked on all rows for the properties that
+hold at any size.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import gated_deltanet_chunked_gdr_gb300 as gdr  # noqa: E402
+import oracle  # noqa: E402
+import workloads  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+F32_MAX_ABS, F32_MEAN_REL, BF16_MAX_ABS = 2e-3, 1e-5, 1.5e-2
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _to(x, dev):
+    return None if x is None else x.to(dev)
+
+
+def _run(inp, out_dtype, dev, stream=None):
+    out = gdr.kkt_solve(_to(inp["k"], dev), _to(inp["g"], dev), _to(inp["beta"], dev),
+                        _to(inp["cu_seqlens"], dev), output_dtype=out_dtype, stream=stream)
+    torch.cuda.synchronize(dev)
+    assert gdr.device_status() == gdr.GDR_OK
+    return out
+
+
+def _metrics(got, ref):
+    d = np.abs(got - ref)
+    return float(d.max()), float(d.sum() / np.abs(ref).sum())
+
+
+def _check(got, ref, out_dtype, what=""):
+    max_abs, mean_rel = _metrics(got, ref)
+    assert np.isfinite(got).all(), what
+    if out_dtype == torch.float32:
+        assert max_abs <= F32_MAX_ABS and mean_rel <= F32_MEAN_REL, (what, max_abs, mean_rel)
+    else:
+        assert max_abs <= BF16_MAX_ABS, (what, max_abs, mean_rel)
+    return max_abs, mean_rel
+
+
+def _real_rows(wl):
+    if wl.varlen_lengths is None:
+        return np.arange(wl.B * wl.T)
+    cu = workloads.cu_seqlens_of(wl)
+    return np.arange(int(cu[-1]))
+
+
+def _full_parity(wl, out_dtype, dev):
+    inp = workloads.make_inputs(wl)
+    out = _run(inp, out_dtype, dev)
+    ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], inp["cu_seqlens"])
+    got = out.double().cpu().numpy().reshape(-1, wl.H, 64)
+    rows = _real_rows(wl)
+    return _check(got[rows], ref.reshape(-1, wl.H, 64)[rows], out_dtype, wl.name), out
+
+
+@pytest.mark.parametrize("name,out_dtype", [
+    ("c1", torch.float32), ("c2", torch.float32), ("c3", torch.bfloat16), ("c3", torch.float32),
+    ("c4", torch.float32), ("c1", torch.bfloat16), ("c4", torch.bfloat16)])
+def test_workload_full_parity(name, out_dtype):
+    _full_parity(workloads.CONFIGS[name], out_dtype, _dev())
+
+
+@pytest.mark.parametrize("use_g,use_beta", [(False, True), (True, False), (False, False)])
+def test_none_variants_partial_chunk_odd_heads(use_g, use_beta):
+    wl = workloads.CONFIGS["c2"].with_(use_g=use_g, use_beta=use_beta)
+    _full_parity(wl, torch.float32, _dev())
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 1, 1), (3, 63, 1), (2, 64, 2), (3, 65, 3), (1, 130, 7),
+                                   (2, 191, 4), (1, 64 * 5 + 17, 1)])
+def test_edge_shapes(B, T, H):
+    wl = workloads.Workload(f"edge_{B}_{T}_{H}", B, T, H, 128, "f32", seed=50 + T + H)
+    _full_parity(wl, torch.float32, _dev())
+
+
+def test_varlen_edge_lengths_and_empty_sequence():
+    lens = (1, 64, 0, 65, 128, 2, 63, 200, 0, 129)
+    wl = workloads.Workload("varlen_edges", len(lens), sum(lens), 3, 128, "f32", seed=77,
+                            varlen_lengths=lens)
+    _full_parity(wl, torch.float32, _dev())
+
+
+def test_varlen_equals_separate_runs():
+    dev = _dev()
+    wl = workloads.CONFIGS["c4"]
+    inp = workloads.make_inputs(wl)
+    packed = _run(inp, torch.float32, dev)
+    cu = workloads.cu_seqlens_of(wl)
+    for n in range(wl.B):
+        s, e = int(cu[n]), int(cu[n + 1])
+        one = {"k": inp["k"][:, s:e], "g": inp["g"][:, s:e], "beta": inp["beta"][:, s:e],
+               "cu_seqlens": None}
+        alone = _run(one, torch.float32, dev)
+        assert torch.equal(packed[:, s:e], alone), n
+
+
+def test_steep_gate_within_clamp():
+    # log-gates falling by up to ~0.7 per token: differences down to about -44.
+    dev = _dev()
+    wl = workloads.CONFIGS["c1"]
+    inp = workloads.make_inputs(wl)
+    rng = np.random.default_rng(9)
+    a = -0.7 * rng.random((wl.B * wl.T, wl.H)).astype(np.float32)
+    g = np.empty_like(a)
+    for c0 in range(0, wl.T, 64):
+        g[c0:c0 + 64] = np.cumsum(a[c0:c0 + 64], axis=0, dtype=np.float32)
+    inp["g"] = torch.from_numpy(g).reshape(wl.B, wl.T, wl.H)
+    out = _run(inp, torch.float32, dev)
+    ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"])
+    _check(out.double().cpu().numpy(), ref, torch.float32, "steep gate")
+
+
+def test_bf16_output_is_rounded_fp32_output():
+    dev = _dev()
+    inp = workloads.make_inputs(workloads.CONFIGS["c2"])
+    f32 = _run(inp, torch.float32, dev)
+    bf = _run(inp, torch.bfloat16, dev)
+    assert torch.equal(f32.to(torch.bfloat16), bf)
+
+
+def test_deterministic_and_stream_aware():
+    dev = _dev()
+    inp = workloads.make_inputs(workloads.CONFIGS["c4"])
+    a = _run(inp, torch.float32, dev)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        b = _run(inp, torch.float32, dev, stream=s.cuda_stream)
+    assert torch.equal(a, b)
+
+
+def test_no_writes_outside_real_rows_or_buffer():
+    # Canary: the output view sits inside a larger buffer filled with a
+    # sentinel; cu[B] < T leaves the tail rows unwritten.
+    dev = _dev()
+    lens = (70, 1, 130)
+    T = sum(lens) + 37
+    wl = workloads.Workload("canary", len(lens), T, 5, 128, "f32", seed=5)
+    inp = workloads.make_inputs(wl.with_(varlen_lengths=lens + (37,), B=4))
+    cu = torch.tensor([0, 70, 71, 201], dtype=torch.int32)
+    pad = 4096
+    buf = torch.full((pad + T * 5 * 64 + pad,), 7.25, dtype=torch.float32, device=dev)
+    out = buf[pad:pad + T * 5 * 64].view(1, T, 5, 64)
+    gdr.kkt_solve(inp["k"].to(dev), inp["g"].to(dev), inp["beta"].to(dev), cu.to(dev), out=out)
+    torch.cuda.synchronize(dev)
+    assert gdr.device_status() == gdr.GDR_OK
+    assert torch.all(buf[:pad] == 7.25) and torch.all(buf[-pad:] == 7.25)
+    assert torch.all(out[:, 201:] == 7.25)
+    ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], cu)
+    _check(out[:, :201].double().cpu().numpy(), ref[:, :201], torch.float32, "canary")
+
+
+def test_golden_fixture_rows():
+    import os
+    dev = _dev()
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("make_golden", os.path.join(here, "make_golden.py"))
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    inp = workloads.make_inputs(mg.WL)
+    out = _run(inp, torch.float32, dev).double().cpu().numpy().reshape(-1, mg.WL.H, 64)
+    got, want = [], []
+    for line in open(os.path.join(here, "oracle_small.txt")):
+        if line.startswith("#"):
+            continue
+        parts = line.split()
+        r, h = int(parts[0]), int(parts[1])
+        got.append(out[r, h])
+        want.append(np.array([float(v) for v in parts[2:]]))
+    _check(np.array(got), np.array(want), torch.float32, "golden")
+
+
+def test_full_size_bf16_sampled_parity_and_invariants():
+    dev = _dev()
+    wl = workloads.CONFIGS["c5"]
+    inp = workloads.make_inputs(wl)
+    out = _run(inp, torch.bfloat16, dev)
+    flat = out.view(-1, wl.H, 64)
+    # Properties on every row: finite, unit diagonal, zero strictly-upper part.
+    assert torch.isfinite(flat).all()
+    loc = torch.arange(wl.T, device=dev).remainder(64).repeat(wl.B)       # row within chunk
+    cols = torch.arange(64, device=dev)
+    diag = flat.gather(2, loc.view(-1, 1, 1).expand(-1, wl.H, 1)).squeeze(-1)
+    assert torch.all(diag == 1)
+    upper = cols.view(1, 1, 64) > loc.view(-1, 1, 1)
+    assert torch.all(flat.masked_select(upper) == 0)
+    # Sampled tiles against the oracle.
+    tiles = workloads.sample_tiles(wl, 256)
+    refs = oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], tiles)
+    got = np.concatenate([flat[r0:r0 + L, h].double().cpu().numpy() for (_, _, h, r0, L) in tiles])
+    _check(got, np.concatenate(refs), torch.bfloat16, "c5 sampled")
