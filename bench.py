@@ -57,6 +57,22 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def reduce_max(x: float, ws: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when ws == 1)."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(token_heads_per_rank: int, ms_per_step_max: float, ws: int) -> float:
+    """Whole-job throughput: every rank processes its own copy of the workload."""
+    return ws * token_heads_per_rank / (ms_per_step_max * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -259,14 +275,10 @@ def main():
     torch.cuda.synchronize(dev)
     barrier()
     clocks = sampler.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(ev0.elapsed_time(ev1), ws, dev)
     ms_step = ms_total / args.steps
     th_rank = wl.token_heads
-    value = ws * th_rank / (ms_step * 1e-3)
+    value = aggregate_value(th_rank, ms_step, ws)
     if gdr.device_status() != gdr.GDR_OK:
         raise RuntimeError("device status not ok after the timed region")
 
@@ -299,11 +311,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.e2e_steps, ws, dev)
     barrier()
 
     if rank == 0:
@@ -335,7 +343,7 @@ def main():
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                          "bytes_per_token_head": bpt},
-            "e2e": {"value": ws * th_rank / (e2e_ms * 1e-3), "unit": UNIT,
+            "e2e": {"value": aggregate_value(th_rank, e2e_ms, ws), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,

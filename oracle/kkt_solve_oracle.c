@@ -28,8 +28,8 @@
  * Readings where the pages are silent: beta scales row i; the exponent is not
  *   clamped here (the Ascend kernel clamps it to [-50, 50], which never binds
  *   for chunk-local decays); g = NULL means g = 0, beta = NULL means beta = 1.
- * Parity of this oracle to the pages' own implementation is unpinned (the pages
- * print no output values); its pins are the mathematical ones in the tests.
+ * The pages print no output values, so the oracle is pinned by mathematics:
+ * closed forms, brute-force inversion and invariants (tests/test_oracle_pins.py).
  */
 #include <math.h>
 #include <stdint.h>
