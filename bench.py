@@ -57,6 +57,28 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def kernel_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ("gated_deltanet_chunked_gdr_gb300/csrc/gdr_kkt_solve.cu", "include/gdr_kkt_solve.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(wl, out_dtype: str):
+    """DRAM bytes per launch (read + write) from the committed ncu summary, or
+    None when it was taken on another kernel source or another workload."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(f"{wl.name}:{out_dtype}")
+    if not d or d.get("source_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
 def reduce_max(x: float, ws: int, device=None) -> float:
     """Max of a per-rank float over all ranks (identity when ws == 1)."""
     if ws <= 1:
@@ -318,14 +340,7 @@ def main():
         peak, peak_kind = measured_peaks()
         bpt = bytes_per_token_head(wl, out_dtype)
         achieved = th_rank * bpt / (ms_step * 1e-3) / 1e9
-        traffic = None
-        tpath = os.path.join(ROOT, "profiles", "traffic.json")
-        if os.path.exists(tpath):
-            with open(tpath) as f:
-                tj = json.load(f)
-            key = f"{wl.name}:{out_dtype}"
-            if key in tj:
-                traffic = tj[key]
+        traffic = recorded_traffic(wl, out_dtype)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,

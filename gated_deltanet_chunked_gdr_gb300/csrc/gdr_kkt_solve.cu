@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             named_bar_sync(bar_id, 128);                       // B3: A complete
 
             // ---- solve: lane -> (tile, row c) of block s
-            const int sblk = (qd + r) & 3;
+            const int sblk = (qd + r + wg) & 3;     // heavy blocks of the 3 warpgroups sit on different SM sub-partitions
             const int tt = lane >> 4;
             const int c = 16 * sblk + (lane & 15);
             const float *A = reinterpret_cast<const float *>(abuf + (tt ? kATile1Off : 0));
