@@ -59,7 +59,7 @@ constexpr int kAPitch = 68;                         // floats per A row (68*4 = 
 constexpr int kATileBytes = kChunk * kAPitch * 4;   // 17408
 constexpr int kATile1Off = kATileBytes + 16;        // second tile shifted by 16 B (other banks)
 constexpr int kAWGBytes = 34944;                    // >= kATile1Off + kATileBytes, multiple of 128
-constexpr int kGWGBytes = 2 * 2 * kChunk * 4;       // g of two tiles, double buffered
+constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
 constexpr uint32_t kTmemCols = 512;
 
 constexpr int kOffK = 0;
@@ -253,19 +253,34 @@ __device__ __forceinline__ Tile tile_of(const Params &p, int64_t u) {
     return t;
 }
 
-// ---------------------------------------------------------------- the solve
-// Right-looking substitution for row c of (I + A)^{-1}.  y[j] accumulates
-// -sum_{i>j} A[i][j] * y[i]; processing i from the top down, y[i] becomes final
-// (plus 1 on the diagonal) and is pushed into every y[j], j < i.  Rows i above
-// c give y[i] = 0, so one instruction stream serves all 16 rows of a block.
-template <int TOP>
-__device__ __forceinline__ void solve_rows(float (&y)[64], const float *A, int c) {
+// ------------------------------------------------------------- the inverse
+// X = (I + A)^{-1} is built from 16x16 blocks (the page's BC = 16 sub-blocks):
+//   D_II = (I + A_II)^{-1}                       for the four diagonal blocks,
+//   X_IJ = -D_II * sum_{M=J}^{I-1} A_IM X_MJ     for the six blocks below them.
+// The diagonal blocks use fp32 forward substitution on CUDA cores (one lane per
+// row).  The off-diagonal products run on tensor cores as 3xTF32 mma.sync
+// (x = big + small, both tf32; big*big + big*small + small*big), which keeps
+// them fp32-accurate.  They are evaluated transposed, Z_JI = X_IJ^T =
+// -(sum_M Z_JM A_IM^T) D_II^T, so every product's left operand is the previous
+// product's accumulator.
+
+// Diagonal inverses are parked in the free upper blocks of the A buffer:
+// D_00 -> block (0,1), D_11 -> (0,2), D_22 -> (0,3), D_33 -> (1,2).
+__device__ __forceinline__ int dslot_r(int I) { return I == 3 ? 1 : 0; }
+__device__ __forceinline__ int dslot_c(int I) { return I == 3 ? 2 : I + 1; }
+
+// Row c of D_II by right-looking substitution inside block (I, I): y[j]
+// accumulates -sum_{i>j} A[i][j] y[i]; processing i downwards, y[i] is final
+// (plus 1 on the diagonal) when reached.  Rows above c give y = 0.
+__device__ __forceinline__ void diag_inverse_row(const float *Ab, int c, float (&y)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) y[j] = 0.0f;
 #pragma unroll
     for (int ii = 0; ii < 16; ++ii) {
-        const int i = TOP - ii;
+        const int i = 15 - ii;
         y[i] += (i == c) ? 1.0f : 0.0f;
         const float yi = y[i];
-        const float4 *Ar = reinterpret_cast<const float4 *>(A + i * kAPitch);
+        const float4 *Ar = reinterpret_cast<const float4 *>(Ab + i * kAPitch);
 #pragma unroll
         for (int j4 = 0; j4 < (i + 3) / 4; ++j4) {
             const float4 a = Ar[j4];
@@ -274,6 +289,115 @@ __device__ __forceinline__ void solve_rows(float (&y)[64], const float *A, int c
             if (4 * j4 + 2 < i) y[4 * j4 + 2] = fmaf(-a.z, yi, y[4 * j4 + 2]);
             if (4 * j4 + 3 < i) y[4 * j4 + 3] = fmaf(-a.w, yi, y[4 * j4 + 3]);
         }
+    }
+}
+
+// A 16x16 fp32 left operand in m16n8k8 A-fragment layout for both k8 steps,
+// split into tf32 big and small parts.  Inside each k8 step the k order is
+// permuted (logical k = t -> column 2t, k = t + 4 -> column 2t + 1); with that
+// order an m16n8 accumulator pair is already a left operand.  Every right
+// operand below uses the same order.
+struct Frag16 {
+    uint32_t big[2][4];
+    uint32_t small[2][4];
+};
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t &big, uint32_t &small) {
+    uint32_t b;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(x));
+    big = b;
+    small = __float_as_uint(x - __uint_as_float(b));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void frag_from_acc(const float (&acc)[2][4], Frag16 &f) {
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const float v[4] = {acc[ks][0], acc[ks][2], acc[ks][1], acc[ks][3]};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_tf32(v[e], f.big[ks][e], f.small[ks][e]);
+    }
+}
+
+// acc += F * Bm for a 16x16 right operand Bm read from shared memory: for k8
+// step ks, n8 tile nt and this lane (g = lane / 4, t = lane % 4) the pair
+// (Bm[8ks + 2t][8nt + g], Bm[8ks + 2t + 1][8nt + g]) is the float2 at
+// rowp + (8 nt + g) * kAPitch + 8 ks + 2 t, i.e. Bm is the transpose of the
+// row-major 16x16 block at rowp.
+__device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag16 &f,
+                                                  const float *rowp, int g, int t) {
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float2 b = *reinterpret_cast<const float2 *>(rowp + (8 * nt + g) * kAPitch +
+                                                               8 * ks + 2 * t);
+            uint32_t bb0, bs0, bb1, bs1;
+            split_tf32(b.x, bb0, bs0);
+            split_tf32(b.y, bb1, bs1);
+            mma_tf32(acc[nt], f.small[ks], bb0, bb1);
+            mma_tf32(acc[nt], f.big[ks], bs0, bs1);
+            mma_tf32(acc[nt], f.big[ks], bb0, bb1);
+        }
+    }
+}
+
+// Left operand D_JJ^T (= Z_JJ) read from its parking block.
+__device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag16 &f) {
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const float v[4] = {D[(8 * ks + 2 * t) * kAPitch + g], D[(8 * ks + 2 * t) * kAPitch + g + 8],
+                            D[(8 * ks + 2 * t + 1) * kAPitch + g],
+                            D[(8 * ks + 2 * t + 1) * kAPitch + g + 8]};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_tf32(v[e], f.big[ks][e], f.small[ks][e]);
+    }
+}
+
+// Blocks Z_JI = X_IJ^T for I = J+1..3 of one tile (At = its A buffer).  Split
+// operands are rebuilt when needed instead of cached, to stay within registers.
+template <int J>
+__device__ __forceinline__ void merge_column(const float *At, int g, int t,
+                                             float (&Z)[3 - J][2][4]) {
+#pragma unroll
+    for (int I = J + 1; I < 4; ++I) {
+        float acc[2][4] = {};
+#pragma unroll
+        for (int M = J; M < I; ++M) {
+            Frag16 f;
+            if (M == J) frag_from_dT(At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J), g, t, f);
+            else frag_from_acc(Z[M - J - 1], f);
+            mma3_times_blockT(acc, f, At + 16 * I * kAPitch + 16 * M, g, t);
+        }
+        Frag16 rf;
+        frag_from_acc(acc, rf);
+        float z[2][4] = {};
+        mma3_times_blockT(z, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Z[I - J - 1][nt][e] = -z[nt][e];
+    }
+}
+
+// Writes Z_JI (accumulator layout) into rows 16I.. / columns 16J.. of X.
+__device__ __forceinline__ void store_block_T(float *At, int I, int J, const float (&z)[2][4],
+                                              int g, int t) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        float *r0 = At + (16 * I + 8 * nt + 2 * t) * kAPitch + 16 * J + g;
+        r0[0] = z[nt][0];
+        r0[kAPitch] = z[nt][1];
+        r0[8] = z[nt][2];
+        r0[kAPitch + 8] = z[nt][3];
     }
 }
 
@@ -290,15 +414,39 @@ __device__ __forceinline__ Tile pick(const Tile &a, const Tile &b, bool second) 
     return t;
 }
 
-__device__ __forceinline__ void load_gb(const Params &p, const Tile &t, int i, float &gv,
-                                        float &bv) {
-    gv = 0.0f;
-    bv = 0.0f;
+// Per-row gate inputs of a tile, loaded one pair ahead: this row's g and beta
+// and the chunk's reference log-gate gref = (g_first + g_last) / 2.
+struct RowIn {
+    float g, beta, gref;
+};
+
+__device__ __forceinline__ RowIn load_row(const Params &p, const Tile &t, int i) {
+    RowIn r;
+    r.g = 0.0f;
+    r.beta = 0.0f;
+    r.gref = 0.0f;
     if (i < t.L) {
-        const int64_t idx = (t.row0 + i) * p.H + t.h;
-        gv = p.g ? __ldg(p.g + idx) : 0.0f;
-        bv = p.beta ? __bfloat162float(p.beta[idx]) : 1.0f;
+        const int64_t base = t.row0 * p.H + t.h;
+        if (p.g) {
+            r.g = __ldg(p.g + base + static_cast<int64_t>(i) * p.H);
+            r.gref = 0.5f * (__ldg(p.g + base) + __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H));
+        }
+        r.beta = p.beta ? __bfloat162float(p.beta[base + static_cast<int64_t>(i) * p.H]) : 1.0f;
     }
+    return r;
+}
+
+__device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return out != 0;
 }
 
 template <bool OUT_BF16>
@@ -431,18 +579,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int qd = warp & 3;                 // TMEM lane quadrant of this warp
         const int tt_e = qd >> 1;                // epilogue: tile of this thread's row
         const int i_e = 32 * (qd & 1) + lane;    // epilogue: row within the tile
+        const int tid = threadIdx.x & 127;       // thread index inside the warpgroup
+        const int g8 = lane >> 2, t4 = lane & 3; // mma.sync fragment coordinates
         uint8_t *abuf = smem + kOffA + wg * kAWGBytes;
-        float *gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);
+        float *const At0 = reinterpret_cast<float *>(abuf);
+        float *const At1 = reinterpret_cast<float *>(abuf + kATile1Off);
+        auto At = [At0, At1](int t) { return t ? At1 : At0; };
+        float *gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);   // [parity][tile][64]
+        float *vbuf = gbuf + 2 * 2 * kChunk;                                       // [parity][tile][64]
         const int bar_id = 1 + wg;
 
         int64_t q = wg;
         Tile cur0 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x));
         Tile cur1 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x) + 1);
-        float gv, bv;
-        load_gb(p, pick(cur0, cur1, tt_e), i_e, gv, bv);
+        RowIn rin = load_row(p, pick(cur0, cur1, tt_e), i_e);
 
         for (int r = 0; q < n_local; ++r, q += kNumWG) {
-            // Prefetch the next pair's schedule and g/beta.
+            // Prefetch the next pair's schedule and row inputs.
             const int64_t qn = q + kNumWG;
             Tile nx0, nx1;
             nx0.L = nx1.L = 0;
@@ -452,17 +605,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 nx0 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x));
                 nx1 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x) + 1);
             }
-            float gn, bn;
-            load_gb(p, pick(nx0, nx1, tt_e), i_e, gn, bn);
+            const RowIn rnext = load_row(p, pick(nx0, nx1, tt_e), i_e);
 
             if (qd == 0 && lane == 0) {
                 int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
                 wg_flag[wg] = ok;
             }
-            float *gcur = gbuf + (r & 1) * 2 * kChunk;
-            gcur[tt_e * kChunk + i_e] = gv;
-            named_bar_sync(bar_id, 128);                       // B2: g ready, A free
+            // Gate factors around the chunk's reference: exp(g_i - g_j) =
+            // u_i * v_j with u_i = exp(g_i - gref), v_j = exp(gref - g_j).  Used
+            // only when every |g - gref| <= 30 in both tiles (no overflow, and
+            // the [-50, 50] clamp cannot bind); otherwise the clamped
+            // exp(g_i - g_j) is evaluated directly.
+            const Tile te = pick(cur0, cur1, tt_e);
+            const bool rowok = i_e < te.L;
+            float ui = 1.0f, vi = 1.0f;
+            bool unsafe = false;
+            if (p.g && rowok) {
+                const float d = rin.g - rin.gref;
+                unsafe = !(fabsf(d) <= 30.0f);
+                ui = expf(d);
+                vi = expf(-d);
+            }
+            float *gcur = gbuf + (r & 1) * 2 * kChunk + tt_e * kChunk;
+            float *vcur = vbuf + (r & 1) * 2 * kChunk + tt_e * kChunk;
+            gcur[i_e] = rin.g;
+            vcur[i_e] = rowok ? vi : 0.0f;
+            const bool direct = named_bar_red_or(bar_id, 128, unsafe);   // B2: g, v ready; A free
             if (!wg_flag[wg]) break;
             tc_fence_after();
 
@@ -484,113 +653,138 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
 
-                const Tile te = pick(cur0, cur1, tt_e);
-                float *Arow = reinterpret_cast<float *>(abuf + (tt_e ? kATile1Off : 0)) +
-                              i_e * kAPitch;
-                const float *gt = gcur + tt_e * kChunk;
-                if (i_e < te.L) {
-                    const float gi = gv;
-                    const float bi = bv;
-                    if ((qd & 1) == 0) {
+                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + i_e * kAPitch);
+                // Rows 0..31 only need columns j < 32 (A is strictly lower).
+                const int n4 = (qd & 1) ? 16 : 8;
+                if (!rowok) {
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 gj = *reinterpret_cast<const float4 *>(gt + 4 * j4);
-                            float4 a;
-                            a.x = bi * __uint_as_float(sr[4 * j4 + 0]) *
-                                  __expf(fminf(fmaxf(gi - gj.x, -50.f), 50.f));
-                            a.y = bi * __uint_as_float(sr[4 * j4 + 1]) *
-                                  __expf(fminf(fmaxf(gi - gj.y, -50.f), 50.f));
-                            a.z = bi * __uint_as_float(sr[4 * j4 + 2]) *
-                                  __expf(fminf(fmaxf(gi - gj.z, -50.f), 50.f));
-                            a.w = bi * __uint_as_float(sr[4 * j4 + 3]) *
-                                  __expf(fminf(fmaxf(gi - gj.w, -50.f), 50.f));
-                            reinterpret_cast<float4 *>(Arow)[j4] = a;
-                        }
-                    } else {
+                    for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = z;
+                } else if (!direct) {
+                    const float w = rin.beta * ui;
 #pragma unroll
-                        for (int j4 = 0; j4 < 16; ++j4) {
-                            const float4 gj = *reinterpret_cast<const float4 *>(gt + 4 * j4);
+                    for (int j4 = 0; j4 < 16; ++j4) {
+                        if (j4 < n4) {
+                            const float4 v = reinterpret_cast<const float4 *>(vcur)[j4];
                             float4 a;
-                            a.x = bi * __uint_as_float(sr[4 * j4 + 0]) *
-                                  __expf(fminf(fmaxf(gi - gj.x, -50.f), 50.f));
-                            a.y = bi * __uint_as_float(sr[4 * j4 + 1]) *
-                                  __expf(fminf(fmaxf(gi - gj.y, -50.f), 50.f));
-                            a.z = bi * __uint_as_float(sr[4 * j4 + 2]) *
-                                  __expf(fminf(fmaxf(gi - gj.z, -50.f), 50.f));
-                            a.w = bi * __uint_as_float(sr[4 * j4 + 3]) *
-                                  __expf(fminf(fmaxf(gi - gj.w, -50.f), 50.f));
-                            reinterpret_cast<float4 *>(Arow)[j4] = a;
+                            a.x = (__uint_as_float(sr[4 * j4 + 0]) * w) * v.x;
+                            a.y = (__uint_as_float(sr[4 * j4 + 1]) * w) * v.y;
+                            a.z = (__uint_as_float(sr[4 * j4 + 2]) * w) * v.z;
+                            a.w = (__uint_as_float(sr[4 * j4 + 3]) * w) * v.w;
+                            Arow[j4] = a;
                         }
                     }
                 } else {
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float gi = rin.g, bi = rin.beta;
 #pragma unroll
-                    for (int j4 = 0; j4 < 16; ++j4) reinterpret_cast<float4 *>(Arow)[j4] = z;
+                    for (int j4 = 0; j4 < 16; ++j4) {
+                        if (j4 < n4) {
+                            const float4 gj = reinterpret_cast<const float4 *>(gcur)[j4];
+                            float4 a;
+                            a.x = bi * __uint_as_float(sr[4 * j4 + 0]) *
+                                  __expf(fminf(fmaxf(gi - gj.x, -50.f), 50.f));
+                            a.y = bi * __uint_as_float(sr[4 * j4 + 1]) *
+                                  __expf(fminf(fmaxf(gi - gj.y, -50.f), 50.f));
+                            a.z = bi * __uint_as_float(sr[4 * j4 + 2]) *
+                                  __expf(fminf(fmaxf(gi - gj.z, -50.f), 50.f));
+                            a.w = bi * __uint_as_float(sr[4 * j4 + 3]) *
+                                  __expf(fminf(fmaxf(gi - gj.w, -50.f), 50.f));
+                            Arow[j4] = a;
+                        }
+                    }
                 }
             }
             named_bar_sync(bar_id, 128);                       // B3: A complete
 
-            // ---- solve: lane -> (tile, row c) of block s
-            const int sblk = (qd + r + wg) & 3;     // heavy blocks of the 3 warpgroups sit on different SM sub-partitions
-            const int tt = lane >> 4;
-            const int c = 16 * sblk + (lane & 15);
-            const float *A = reinterpret_cast<const float *>(abuf + (tt ? kATile1Off : 0));
-            float y[64];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) y[j] = 0.0f;
-            if (sblk == 3) solve_rows<63>(y, A, c);
-            if (sblk >= 2) solve_rows<47>(y, A, c);
-            if (sblk >= 1) solve_rows<31>(y, A, c);
-            solve_rows<15>(y, A, c);
-            named_bar_sync(bar_id, 128);                       // B4: A no longer read
-
-            // ---- store: stage own rows in the A buffer, then coalesced 16-B stores
+            // ---- diagonal inverses: thread -> (tile, block I, row c)
+            const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
+            float drow[16];
+            diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
             {
-                uint8_t *rowp = abuf + (tt ? kATile1Off : 0) + c * (kAPitch * 4);
+                float4 *dst = reinterpret_cast<float4 *>(At(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
+                                                         16 * dslot_c(dI));
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4)
+                    dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
+            }
+            named_bar_sync(bar_id, 128);                       // B3b: D blocks ready
+
+            // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column);
+            //      then X rows are assembled in the A buffer (after B4 in both branches)
+            const int mt = qd & 1;
+            if (qd < 2) {
+                float z0[3][2][4];
+                merge_column<0>(At(mt), g8, t4, z0);
+                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
+                store_block_T(At(mt), 1, 0, z0[0], g8, t4);
+                store_block_T(At(mt), 2, 0, z0[1], g8, t4);
+                store_block_T(At(mt), 3, 0, z0[2], g8, t4);
+            } else {
+                float z1[2][2][4], z2[1][2][4];
+                merge_column<1>(At(mt), g8, t4, z1);
+                merge_column<2>(At(mt), g8, t4, z2);
+                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
+                store_block_T(At(mt), 2, 1, z1[0], g8, t4);
+                store_block_T(At(mt), 3, 1, z1[1], g8, t4);
+                store_block_T(At(mt), 3, 2, z2[0], g8, t4);
+            }
+            {
+                float4 *row = reinterpret_cast<float4 *>(At(dt) + (16 * dI + dc) * kAPitch);
+                row[4 * dI + 0] = make_float4(drow[0], drow[1], drow[2], drow[3]);
+                row[4 * dI + 1] = make_float4(drow[4], drow[5], drow[6], drow[7]);
+                row[4 * dI + 2] = make_float4(drow[8], drow[9], drow[10], drow[11]);
+                row[4 * dI + 3] = make_float4(drow[12], drow[13], drow[14], drow[15]);
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int j4 = 4; j4 < 16; ++j4)
+                    if (j4 >= 4 * dI + 4) row[j4] = z;
+            }
+            named_bar_sync(bar_id, 128);                       // B5: X complete
+
+            // ---- coalesced 16-byte stores: warp -> 32 rows of one tile
+            {
+                const int st_t = qd >> 1;
+                const Tile ts = pick(cur0, cur1, st_t);
+                const float *Xs = At(st_t);
                 if (OUT_BF16) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        uint4 v;
-                        __nv_bfloat162 b0 = __floats2bfloat162_rn(y[8 * q4 + 0], y[8 * q4 + 1]);
-                        __nv_bfloat162 b1 = __floats2bfloat162_rn(y[8 * q4 + 2], y[8 * q4 + 3]);
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(y[8 * q4 + 4], y[8 * q4 + 5]);
-                        __nv_bfloat162 b3 = __floats2bfloat162_rn(y[8 * q4 + 6], y[8 * q4 + 7]);
-                        v.x = *reinterpret_cast<uint32_t *>(&b0);
-                        v.y = *reinterpret_cast<uint32_t *>(&b1);
-                        v.z = *reinterpret_cast<uint32_t *>(&b2);
-                        v.w = *reinterpret_cast<uint32_t *>(&b3);
-                        reinterpret_cast<uint4 *>(rowp)[q4] = v;
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = 32 * (qd & 1) + 4 * it + (lane >> 3);
+                        const int piece = lane & 7;
+                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece);
+                        const float4 b = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece + 4);
+                        if (rr < ts.L) {
+                            __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y);
+                            __nv_bfloat162 h1 = __floats2bfloat162_rn(a.z, a.w);
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y);
+                            __nv_bfloat162 h3 = __floats2bfloat162_rn(b.z, b.w);
+                            uint4 v;
+                            v.x = *reinterpret_cast<uint32_t *>(&h0);
+                            v.y = *reinterpret_cast<uint32_t *>(&h1);
+                            v.z = *reinterpret_cast<uint32_t *>(&h2);
+                            v.w = *reinterpret_cast<uint32_t *>(&h3);
+                            const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 128 +
+                                                       16 * piece) = v;
+                        }
                     }
                 } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 16; ++q4)
-                        reinterpret_cast<float4 *>(rowp)[q4] =
-                            make_float4(y[4 * q4 + 0], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
-                }
-                __syncwarp();
-                constexpr int kChunksPerRow = OUT_BF16 ? 8 : 16;      // 16-byte pieces per row
-                constexpr int kRowsPerIter = 32 / kChunksPerRow;
-#pragma unroll
-                for (int it = 0; it < 32 / kRowsPerIter; ++it) {
-                    const int rho = it * kRowsPerIter + lane / kChunksPerRow;   // 0..31
-                    const int piece = lane % kChunksPerRow;
-                    const int tts = rho >> 4;
-                    const int cs = 16 * sblk + (rho & 15);
-                    const Tile ts = pick(cur0, cur1, tts);
-                    const uint4 v = *reinterpret_cast<const uint4 *>(
-                        abuf + (tts ? kATile1Off : 0) + cs * (kAPitch * 4) + 16 * piece);
-                    if (cs < ts.L) {
-                        const int64_t row = (ts.row0 + cs) * p.H + ts.h;
-                        uint8_t *dst = reinterpret_cast<uint8_t *>(p.out) +
-                                       row * (OUT_BF16 ? 128 : 256) + 16 * piece;
-                        *reinterpret_cast<uint4 *>(dst) = v;
+                    for (int it = 0; it < 16; ++it) {
+                        const int rr = 32 * (qd & 1) + 2 * it + (lane >> 4);
+                        const int piece = lane & 15;
+                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 4 * piece);
+                        if (rr < ts.L) {
+                            const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
+                            *reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 256 +
+                                                        16 * piece) = a;
+                        }
                     }
                 }
             }
             cur0 = nx0;
             cur1 = nx1;
-            gv = gn;
-            bv = bn;
+            rin = rnext;
         }
     }
 
