@@ -128,6 +128,41 @@ def test_steep_gate_within_clamp():
     _check(out.double().cpu().numpy(), ref, torch.float32, "steep gate")
 
 
+def _with_gate(wl, per_token, seed):
+    inp = workloads.make_inputs(wl)
+    rng = np.random.default_rng(seed)
+    a = per_token(rng, (wl.B * wl.T, wl.H)).astype(np.float32)
+    g = np.empty_like(a)
+    for b in range(wl.B):
+        for c0 in range(b * wl.T, (b + 1) * wl.T, 64):
+            c1 = min(c0 + 64, (b + 1) * wl.T)
+            g[c0:c1] = np.cumsum(a[c0:c1], axis=0, dtype=np.float32)
+    inp["g"] = torch.from_numpy(g).reshape(wl.B, wl.T, wl.H)
+    return inp
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gate_range_beyond_factorisation_guard(out_dtype):
+    # Decays up to 2 per token: a chunk's log-gate spans ~64, beyond the range
+    # where exp(g_i - g_j) is factored, so the direct clamped form runs.
+    dev = _dev()
+    wl = workloads.CONFIGS["c2"]
+    inp = _with_gate(wl, lambda rng, sh: -2.0 * rng.random(sh), 31)
+    out = _run(inp, out_dtype, dev)
+    ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"])
+    _check(out.double().cpu().numpy(), ref, out_dtype, "steep decay")
+
+
+def test_non_monotone_gate():
+    # Log-gates that rise and fall inside a chunk (|steps| <= 0.3).
+    dev = _dev()
+    wl = workloads.CONFIGS["c1"]
+    inp = _with_gate(wl, lambda rng, sh: rng.uniform(-0.3, 0.3, sh), 32)
+    out = _run(inp, torch.float32, dev)
+    ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"])
+    _check(out.double().cpu().numpy(), ref, torch.float32, "non-monotone gate")
+
+
 def test_bf16_output_is_rounded_fp32_output():
     dev = _dev()
     inp = workloads.make_inputs(workloads.CONFIGS["c2"])
