@@ -76,6 +76,29 @@ static_assert(kOffA % 1024 == 0, "stages must keep 1024-byte alignment");
 
 constexpr uint64_t kWaitNs = 2000000000ull;         // 2 s bound for every wait
 
+// Division by an invariant divisor d >= 1 for numerators n < 2^31 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994): with
+// l = ceil(log2 d) and m = ceil(2^(31+l) / d), floor(n / d) = (n * m) >> (31 + l);
+// m < 2^33, so the product fits in 64 bits.
+struct FastDiv {
+    uint64_t m;
+    uint32_t shift;
+    uint32_t d;
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        return static_cast<uint32_t>((static_cast<uint64_t>(n) * m) >> shift);
+    }
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    FastDiv f;
+    f.d = d;
+    f.shift = 31 + l;
+    f.m = ((uint64_t(1) << f.shift) + d - 1) / d;
+    return f;
+}
+
 struct Params {
     const float *g;
     const __nv_bfloat16 *beta;
@@ -85,6 +108,8 @@ struct Params {
     int64_t n_slots;   // chunk slots: fixed-length B*NT, varlen floor((T + 63 B)/64)
     int64_t NT;        // chunks per sequence (fixed-length)
     int64_t n_pairs;   // ceil(n_slots * H / 2)
+    FastDiv divH;      // tile -> (slot, head)
+    FastDiv divNT;     // slot -> (sequence, chunk), fixed-length
     int *status;
 };
 
@@ -223,14 +248,15 @@ __device__ __forceinline__ Tile tile_of(const Params &p, int64_t u) {
     Tile t;
     t.row0 = 0;
     t.L = 0;
-    t.h = static_cast<int>(u % p.H);
-    const int64_t slot = u / p.H;
-    if (slot >= p.n_slots) return t;
+    const uint32_t uu = static_cast<uint32_t>(u);          // u < 2^31 (checked on the host)
+    const uint32_t slot = p.divH.div(uu);
+    t.h = static_cast<int>(uu - slot * p.divH.d);
+    if (slot >= static_cast<uint64_t>(p.n_slots)) return t;
     if (p.cu == nullptr) {
-        const int64_t b = slot / p.NT;
-        const int64_t c = slot - b * p.NT;
-        t.row0 = b * p.T + c * kChunk;
-        const int64_t rem = p.T - c * kChunk;
+        const uint32_t b = p.divNT.div(slot);
+        const uint32_t c = slot - b * p.divNT.d;
+        t.row0 = static_cast<int64_t>(b) * p.T + static_cast<int64_t>(c) * kChunk;
+        const int64_t rem = p.T - static_cast<int64_t>(c) * kChunk;
         t.L = static_cast<int>(rem < kChunk ? rem : kChunk);
         return t;
     }
@@ -245,7 +271,7 @@ __device__ __forceinline__ Tile tile_of(const Params &p, int64_t u) {
     const int64_t s = __ldg(p.cu + lo);
     int64_t e = __ldg(p.cu + lo + 1);
     if (e > p.T) e = p.T;
-    const int64_t c = slot - ((s + 63 * lo) >> 6);
+    const int64_t c = static_cast<int64_t>(slot) - ((s + 63 * lo) >> 6);
     const int64_t r0 = s + c * kChunk;
     if (c < 0 || s < 0 || r0 >= e) return t;
     t.row0 = r0;
@@ -916,7 +942,10 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
     prm.H = H;
     prm.NT = (T + kChunk - 1) / kChunk;
     prm.n_slots = cu_seqlens ? (T + 63 * B) / kChunk : B * prm.NT;
+    if (prm.n_slots * H >= (int64_t(1) << 31)) return GDR_ERR_SHAPE;
     prm.n_pairs = (prm.n_slots * H + 1) / 2;
+    prm.divH = make_fastdiv(static_cast<uint32_t>(H));
+    prm.divNT = make_fastdiv(static_cast<uint32_t>(prm.NT));
     int *status_ptr = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status_ptr), g_status_word) != cudaSuccess) {
         cudaGetLastError();
