@@ -58,7 +58,8 @@ constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][1
 constexpr int kAPitch = 68;                         // floats per A row (68*4 = 272 B)
 constexpr int kATileBytes = kChunk * kAPitch * 4;   // 17408
 constexpr int kATile1Off = kATileBytes + 16;        // second tile shifted by 16 B (other banks)
-constexpr int kAWGBytes = 34944;                    // >= kATile1Off + kATileBytes, multiple of 128
+constexpr int kAWGBytes = 35840;                    // >= kATile1Off + kATileBytes, multiple of 1024
+constexpr int kStage1Off = 17408;                   // output staging of the second tile (1024-aligned)
 constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
 constexpr uint32_t kTmemCols = 512;
 
@@ -357,9 +358,31 @@ __device__ __forceinline__ void frag_from_acc(const float (&acc)[2][4], Frag16 &
 // step ks, n8 tile nt and this lane (g = lane / 4, t = lane % 4) the pair
 // (Bm[8ks + 2t][8nt + g], Bm[8ks + 2t + 1][8nt + g]) is the float2 at
 // rowp + (8 nt + g) * kAPitch + 8 ks + 2 t, i.e. Bm is the transpose of the
-// row-major 16x16 block at rowp.
-__device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag16 &f,
-                                                  const float *rowp, int g, int t) {
+// row-major 16x16 block at rowp.  The three split terms accumulate into
+// separate registers (acc.v[0] small*big, [1] big*small, [2] big*big), so the
+// twelve mma.sync of one product form six short independent chains.
+struct Acc3 {
+    float v[3][2][4];
+};
+
+__device__ __forceinline__ void acc3_zero(Acc3 &a) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a.v[i][nt][e] = 0.0f;
+}
+
+__device__ __forceinline__ void acc3_sum(const Acc3 &a, float (&out)[2][4]) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) out[nt][e] = a.v[2][nt][e] + (a.v[0][nt][e] + a.v[1][nt][e]);
+}
+
+__device__ __forceinline__ void mma3_times_blockT(Acc3 &acc, const Frag16 &f, const float *rowp,
+                                                  int g, int t) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
@@ -369,9 +392,9 @@ __device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag
             uint32_t bb0, bs0, bb1, bs1;
             split_tf32(b.x, bb0, bs0);
             split_tf32(b.y, bb1, bs1);
-            mma_tf32(acc[nt], f.small[ks], bb0, bb1);
-            mma_tf32(acc[nt], f.big[ks], bs0, bs1);
-            mma_tf32(acc[nt], f.big[ks], bb0, bb1);
+            mma_tf32(acc.v[0][nt], f.small[ks], bb0, bb1);
+            mma_tf32(acc.v[1][nt], f.big[ks], bs0, bs1);
+            mma_tf32(acc.v[2][nt], f.big[ks], bb0, bb1);
         }
     }
 }
@@ -388,44 +411,118 @@ __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag1
     }
 }
 
-// Blocks Z_JI = X_IJ^T for I = J+1..3 of one tile (At = its A buffer).  Split
-// operands are rebuilt when needed instead of cached, to stay within registers.
-template <int J>
-__device__ __forceinline__ void merge_column(const float *At, int g, int t,
-                                             float (&Z)[3 - J][2][4]) {
+// Blocks Z_JI = X_IJ^T for I = J+1..3 of one tile (At = its A buffer), stored in
+// Z[OFF + I - J - 1].  Split operands are rebuilt when needed instead of cached,
+// to stay within registers.
+template <int J, int OFF>
+__device__ __forceinline__ void merge_column(const float *At, int g, int t, float (&Z)[3][2][4]) {
 #pragma unroll
     for (int I = J + 1; I < 4; ++I) {
-        float acc[2][4] = {};
+        Acc3 acc;
+        acc3_zero(acc);
 #pragma unroll
         for (int M = J; M < I; ++M) {
             Frag16 f;
             if (M == J) frag_from_dT(At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J), g, t, f);
-            else frag_from_acc(Z[M - J - 1], f);
+            else frag_from_acc(Z[OFF + M - J - 1], f);
             mma3_times_blockT(acc, f, At + 16 * I * kAPitch + 16 * M, g, t);
         }
+        float r[2][4];
+        acc3_sum(acc, r);
         Frag16 rf;
-        frag_from_acc(acc, rf);
-        float z[2][4] = {};
-        mma3_times_blockT(z, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
+        frag_from_acc(r, rf);
+        acc3_zero(acc);
+        mma3_times_blockT(acc, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
+        float z[2][4];
+        acc3_sum(acc, z);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) Z[I - J - 1][nt][e] = -z[nt][e];
+            for (int e = 0; e < 4; ++e) Z[OFF + I - J - 1][nt][e] = -z[nt][e];
     }
 }
 
-// Writes Z_JI (accumulator layout) into rows 16I.. / columns 16J.. of X.
-__device__ __forceinline__ void store_block_T(float *At, int I, int J, const float (&z)[2][4],
+// ------------------------------------------------------------ output staging
+// X is assembled in the layout a 128-byte-swizzled TMA store reads: a tile's 64
+// rows of 128 bytes (bf16: 64 values; fp32: two 32-value halves 8 KB apart), the
+// 16-byte piece q of row r stored at piece position q ^ (r % 8).
+template <bool BF16>
+__device__ __forceinline__ uint32_t stage_piece_off(int r, int q) {
+    if (BF16) return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
+    return static_cast<uint32_t>((q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4));
+}
+
+template <bool BF16>
+__device__ __forceinline__ void stage_put(uint8_t *st, int r, int c, float v) {
+    if (BF16) {
+        *reinterpret_cast<__nv_bfloat16 *>(st + stage_piece_off<true>(r, c >> 3) + 2 * (c & 7)) =
+            __float2bfloat16_rn(v);
+    } else {
+        *reinterpret_cast<float *>(st + stage_piece_off<false>(r, c >> 2) + 4 * (c & 3)) = v;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Row r of X restricted to columns >= 16 I: the diagonal block row (d[0..3] =
+// 16 values) followed by zeros.
+template <bool BF16>
+__device__ __forceinline__ void stage_diag_row(uint8_t *st, int r, int I, const float4 (&d)[4]) {
+    if (BF16) {
+        uint4 a, b;
+        a.x = pack_bf16x2(d[0].x, d[0].y); a.y = pack_bf16x2(d[0].z, d[0].w);
+        a.z = pack_bf16x2(d[1].x, d[1].y); a.w = pack_bf16x2(d[1].z, d[1].w);
+        b.x = pack_bf16x2(d[2].x, d[2].y); b.y = pack_bf16x2(d[2].z, d[2].w);
+        b.z = pack_bf16x2(d[3].x, d[3].y); b.w = pack_bf16x2(d[3].z, d[3].w);
+        *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I)) = a;
+        *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I + 1)) = b;
+#pragma unroll
+        for (int q = 2; q < 8; ++q)
+            if (q >= 2 * I + 2) *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, q)) = make_uint4(0, 0, 0, 0);
+    } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4 *>(st + stage_piece_off<false>(r, 4 * I + m)) = d[m];
+#pragma unroll
+        for (int q = 4; q < 16; ++q)
+            if (q >= 4 * I + 4)
+                *reinterpret_cast<float4 *>(st + stage_piece_off<false>(r, q)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Z_JI (accumulator layout) -> rows 16I.. / columns 16J.. of X in the staging.
+template <bool BF16>
+__device__ __forceinline__ void stage_block_T(uint8_t *st, int I, int J, const float (&z)[2][4],
                                               int g, int t) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        float *r0 = At + (16 * I + 8 * nt + 2 * t) * kAPitch + 16 * J + g;
-        r0[0] = z[nt][0];
-        r0[kAPitch] = z[nt][1];
-        r0[8] = z[nt][2];
-        r0[kAPitch + 8] = z[nt][3];
+        const int r0 = 16 * I + 8 * nt + 2 * t, c0 = 16 * J + g;
+        stage_put<BF16>(st, r0, c0, z[nt][0]);
+        stage_put<BF16>(st, r0 + 1, c0, z[nt][1]);
+        stage_put<BF16>(st, r0, c0 + 8, z[nt][2]);
+        stage_put<BF16>(st, r0 + 1, c0 + 8, z[nt][3]);
     }
 }
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 
 __device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag) {
     *abort_flag = 1;
@@ -440,26 +537,36 @@ __device__ __forceinline__ Tile pick(const Tile &a, const Tile &b, bool second) 
     return t;
 }
 
-// Per-row gate inputs of a tile, loaded one pair ahead: this row's g and beta
-// and the chunk's reference log-gate gref = (g_first + g_last) / 2.
+// Per-row gate inputs of a tile, loaded one pair ahead and kept raw (no
+// arithmetic on them until they are used, so the loads stay in flight): this
+// row's g and beta, and the chunk's first and last g.
 struct RowIn {
-    float g, beta, gref;
+    float g, gfirst, glast;
+    unsigned short beta;   // bf16 bits
 };
 
 __device__ __forceinline__ RowIn load_row(const Params &p, const Tile &t, int i) {
     RowIn r;
     r.g = 0.0f;
-    r.beta = 0.0f;
-    r.gref = 0.0f;
+    r.gfirst = 0.0f;
+    r.glast = 0.0f;
+    r.beta = 0;
     if (i < t.L) {
         const int64_t base = t.row0 * p.H + t.h;
         if (p.g) {
             r.g = __ldg(p.g + base + static_cast<int64_t>(i) * p.H);
-            r.gref = 0.5f * (__ldg(p.g + base) + __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H));
+            r.gfirst = __ldg(p.g + base);
+            r.glast = __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H);
         }
-        r.beta = p.beta ? __bfloat162float(p.beta[base + static_cast<int64_t>(i) * p.H]) : 1.0f;
+        r.beta = p.beta ? __ldg(reinterpret_cast<const unsigned short *>(p.beta) + base +
+                                static_cast<int64_t>(i) * p.H)
+                        : static_cast<unsigned short>(0x3F80);   // bf16 1.0
     }
     return r;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(unsigned short b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
 __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
@@ -477,7 +584,8 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
 
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(kNumThreads, 1)
-    kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k, const Params p) {
+    kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_out, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -616,24 +724,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int bar_id = 1 + wg;
 
         int64_t q = wg;
-        Tile cur0 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x));
-        Tile cur1 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x) + 1);
-        RowIn rin = load_row(p, pick(cur0, cur1, tt_e), i_e);
+        RowIn rin = load_row(p, tile_of(p, 2 * (blockIdx.x + q * gridDim.x) + tt_e), i_e);
 
         for (int r = 0; q < n_local; ++r, q += kNumWG) {
-            // Prefetch the next pair's schedule and row inputs.
+            const int64_t pair = blockIdx.x + q * gridDim.x;
+            // Prefetch the next pair's row inputs for this thread's tile.
             const int64_t qn = q + kNumWG;
-            Tile nx0, nx1;
-            nx0.L = nx1.L = 0;
-            nx0.row0 = nx1.row0 = 0;
-            nx0.h = nx1.h = 0;
-            if (qn < n_local) {
-                nx0 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x));
-                nx1 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x) + 1);
-            }
-            const RowIn rnext = load_row(p, pick(nx0, nx1, tt_e), i_e);
+            RowIn rnext;
+            if (qn < n_local) rnext = load_row(p, tile_of(p, 2 * (blockIdx.x + qn * gridDim.x) + tt_e), i_e);
+            else rnext = load_row(p, Tile{0, 0, 0}, i_e);
 
             if (qd == 0 && lane == 0) {
+                bulk_wait_read();          // last pair's TMA stores have read the staging
                 int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
                 wg_flag[wg] = ok;
@@ -643,12 +745,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // only when every |g - gref| <= 30 in both tiles (no overflow, and
             // the [-50, 50] clamp cannot bind); otherwise the clamped
             // exp(g_i - g_j) is evaluated directly.
-            const Tile te = pick(cur0, cur1, tt_e);
-            const bool rowok = i_e < te.L;
+            const bool rowok = i_e < tile_of(p, 2 * pair + tt_e).L;
             float ui = 1.0f, vi = 1.0f;
             bool unsafe = false;
             if (p.g && rowok) {
-                const float d = rin.g - rin.gref;
+                const float d = rin.g - 0.5f * (rin.gfirst + rin.glast);
                 unsafe = !(fabsf(d) <= 30.0f);
                 ui = expf(d);
                 vi = expf(-d);
@@ -687,7 +788,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = z;
                 } else if (!direct) {
-                    const float w = rin.beta * ui;
+                    const float w = bf16_bits_to_float(rin.beta) * ui;
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
@@ -701,7 +802,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                     }
                 } else {
-                    const float gi = rin.g, bi = rin.beta;
+                    const float gi = rin.g, bi = bf16_bits_to_float(rin.beta);
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
@@ -724,9 +825,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
             // ---- diagonal inverses: thread -> (tile, block I, row c)
             const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
-            float drow[16];
-            diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
+            const float4 *dslot = reinterpret_cast<const float4 *>(
+                At(dt) + (16 * dslot_r(dI) + dc) * kAPitch + 16 * dslot_c(dI));
             {
+                float drow[16];
+                diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
                 float4 *dst = reinterpret_cast<float4 *>(At(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
                                                          16 * dslot_c(dI));
 #pragma unroll
@@ -735,83 +838,73 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             named_bar_sync(bar_id, 128);                       // B3b: D blocks ready
 
-            // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column);
-            //      then X rows are assembled in the A buffer (after B4 in both branches)
+            // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column)
             const int mt = qd & 1;
+            float zb[3][2][4];     // Z blocks; see the staging below for their (I, J)
             if (qd < 2) {
-                float z0[3][2][4];
-                merge_column<0>(At(mt), g8, t4, z0);
-                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                store_block_T(At(mt), 1, 0, z0[0], g8, t4);
-                store_block_T(At(mt), 2, 0, z0[1], g8, t4);
-                store_block_T(At(mt), 3, 0, z0[2], g8, t4);
+                merge_column<0, 0>(At(mt), g8, t4, zb);
             } else {
-                float z1[2][2][4], z2[1][2][4];
-                merge_column<1>(At(mt), g8, t4, z1);
-                merge_column<2>(At(mt), g8, t4, z2);
-                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                store_block_T(At(mt), 2, 1, z1[0], g8, t4);
-                store_block_T(At(mt), 3, 1, z1[1], g8, t4);
-                store_block_T(At(mt), 3, 2, z2[0], g8, t4);
+                merge_column<1, 0>(At(mt), g8, t4, zb);
+                merge_column<2, 2>(At(mt), g8, t4, zb);
             }
-            {
-                float4 *row = reinterpret_cast<float4 *>(At(dt) + (16 * dI + dc) * kAPitch);
-                row[4 * dI + 0] = make_float4(drow[0], drow[1], drow[2], drow[3]);
-                row[4 * dI + 1] = make_float4(drow[4], drow[5], drow[6], drow[7]);
-                row[4 * dI + 2] = make_float4(drow[8], drow[9], drow[10], drow[11]);
-                row[4 * dI + 3] = make_float4(drow[12], drow[13], drow[14], drow[15]);
-                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 dv[4];
 #pragma unroll
-                for (int j4 = 4; j4 < 16; ++j4)
-                    if (j4 >= 4 * dI + 4) row[j4] = z;
+            for (int m = 0; m < 4; ++m) dv[m] = dslot[m];
+            named_bar_sync(bar_id, 128);                       // B4: A and D no longer read
+
+            // ---- assemble X in the swizzled staging (reuses the A buffer)
+            {
+                uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
+                // zb[k] holds block (I, J): J=0 warps (1,0),(2,0),(3,0); others (2,1),(3,1),(3,2)
+                const int bI0 = qd < 2 ? 1 : 2, bJ0 = qd < 2 ? 0 : 1;
+                const int bI1 = qd < 2 ? 2 : 3, bJ1 = qd < 2 ? 0 : 1;
+                const int bI2 = 3, bJ2 = qd < 2 ? 0 : 2;
+                stage_block_T<OUT_BF16>(st_m, bI0, bJ0, zb[0], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, bI1, bJ1, zb[1], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, bI2, bJ2, zb[2], g8, t4);
+                stage_diag_row<OUT_BF16>(abuf + (dt ? kStage1Off : 0), 16 * dI + dc, dI, dv);
             }
+            fence_proxy_async_smem();
             named_bar_sync(bar_id, 128);                       // B5: X complete
 
-            // ---- coalesced 16-byte stores: warp -> 32 rows of one tile
+            // ---- store: full chunks by TMA from the staging, partial chunks row by row
+            if (tid == 0) {
+                bool any = false;
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2) {
+                    const Tile ts = tile_of(p, 2 * pair + t2);
+                    if (ts.L == kChunk) {
+                        const uint32_t src = smem_u32(abuf + (t2 ? kStage1Off : 0));
+                        tma_store_3d(&tmap_out, src, 0, ts.h, static_cast<int>(ts.row0));
+                        if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, ts.h, static_cast<int>(ts.row0));
+                        any = true;
+                    }
+                }
+                if (any) bulk_commit();
+            }
             {
                 const int st_t = qd >> 1;
-                const Tile ts = pick(cur0, cur1, st_t);
-                const float *Xs = At(st_t);
-                if (OUT_BF16) {
-#pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = 32 * (qd & 1) + 4 * it + (lane >> 3);
-                        const int piece = lane & 7;
-                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece);
-                        const float4 b = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece + 4);
+                const Tile ts = tile_of(p, 2 * pair + st_t);
+                if (ts.L > 0 && ts.L < kChunk) {
+                    const uint8_t *sb = abuf + (st_t ? kStage1Off : 0);
+                    constexpr int kPieces = OUT_BF16 ? 8 : 16;
+                    constexpr int kRowsPerIt = 32 / kPieces;
+#pragma unroll 2
+                    for (int it = 0; it < 32 / kRowsPerIt; ++it) {
+                        const int rr = 32 * (qd & 1) + kRowsPerIt * it + lane / kPieces;
+                        const int piece = lane % kPieces;
                         if (rr < ts.L) {
-                            __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y);
-                            __nv_bfloat162 h1 = __floats2bfloat162_rn(a.z, a.w);
-                            __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y);
-                            __nv_bfloat162 h3 = __floats2bfloat162_rn(b.z, b.w);
-                            uint4 v;
-                            v.x = *reinterpret_cast<uint32_t *>(&h0);
-                            v.y = *reinterpret_cast<uint32_t *>(&h1);
-                            v.z = *reinterpret_cast<uint32_t *>(&h2);
-                            v.w = *reinterpret_cast<uint32_t *>(&h3);
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sb + stage_piece_off<OUT_BF16>(rr, piece));
                             const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
-                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 128 +
-                                                       16 * piece) = v;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int it = 0; it < 16; ++it) {
-                        const int rr = 32 * (qd & 1) + 2 * it + (lane >> 4);
-                        const int piece = lane & 15;
-                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 4 * piece);
-                        if (rr < ts.L) {
-                            const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
-                            *reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 256 +
-                                                        16 * piece) = a;
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
+                                                       orow * (OUT_BF16 ? 128 : 256) + 16 * piece) = v;
                         }
                     }
                 }
             }
-            cur0 = nx0;
-            cur1 = nx1;
             rin = rnext;
         }
+        if (tid == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -932,6 +1025,19 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GDR_ERR_CUDA;
 
+    CUtensorMap tmap_o;
+    {
+        const int esz = out_dtype == GDR_BF16 ? 2 : 4;
+        const cuuint64_t odims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(ntok)};
+        const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(64 * esz), static_cast<cuuint64_t>(H * 64 * esz)};
+        const cuuint32_t obox[3] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(kChunk)};
+        if (encode(&tmap_o, out_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GDR_ERR_CUDA;
+    }
+
     Params prm;
     prm.g = g;
     prm.beta = static_cast<const __nv_bfloat16 *>(beta);
@@ -956,9 +1062,9 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
     const int64_t grid = prm.n_pairs < sms ? prm.n_pairs : sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (out_dtype == GDR_BF16)
-        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
+        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     else
-        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
+        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }
