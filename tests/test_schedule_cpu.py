@@ -60,3 +60,29 @@ def test_varlen_slots_cover_every_chunk_once(seed):
         assert got == want, (n, lens[n])
         empty_per_seq[n] = (base(cu, n + 1) if n + 1 <= B else n_slots) - base(cu, n) - want
     assert np.all(empty_per_seq >= 0) and np.all(empty_per_seq <= 1)
+
+
+def _fastdiv(d):
+    l = 0
+    while (1 << l) < d:
+        l += 1
+    shift = 31 + l
+    return ((1 << shift) + d - 1) // d, shift
+
+
+@pytest.mark.parametrize("d", [1, 2, 3, 5, 7, 31, 32, 33, 64, 100, 255, 256, 257, 4095, 65537,
+                               (1 << 20) + 1, (1 << 24), (1 << 30) + 3, (1 << 31) - 1])
+def test_multiply_shift_division_by_invariant_divisor(d):
+    # The tile schedule divides numerators n < 2^31 by a fixed d with
+    # m = ceil(2^(31+l) / d), l = ceil(log2 d): floor(n/d) = (n*m) >> (31+l).
+    m, shift = _fastdiv(d)
+    assert m < (1 << 33)
+    rng = np.random.default_rng(d)
+    ns = np.concatenate([rng.integers(0, 1 << 31, size=2000), np.arange(0, 300),
+                         [(1 << 31) - 1, (1 << 31) - 2, d - 1, d, d + 1, 2 * d - 1, 2 * d]])
+    for n in ns:
+        n = int(n)
+        if n >= (1 << 31):
+            continue
+        assert (n * m) >> shift == n // d, (n, d)
+        assert (n * m) < (1 << 64)
