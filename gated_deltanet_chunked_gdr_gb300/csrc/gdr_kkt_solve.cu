@@ -46,8 +46,9 @@ namespace gdr {
 
 constexpr int kChunk = 64;
 constexpr int kHeadK = 128;
-constexpr int kNumWG = 3;
-constexpr int kNumStages = 3;
+constexpr int kNumWG = 2;
+constexpr int kNumStages = 2;
+constexpr int kTilesPerWG = 4;                      // two MMA pairs per warpgroup round
 constexpr int kNumConsumerWarps = 4 * kNumWG;
 constexpr int kProducerWarp = kNumConsumerWarps;
 constexpr int kMmaWarp = kNumConsumerWarps + 1;
@@ -56,11 +57,9 @@ constexpr int kNumThreads = (kNumConsumerWarps + 2) * 32;
 constexpr int kBoxBytes = kChunk * 64 * 2;          // one (tile, K-half) box: 64 rows x 128 B
 constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][128 B] = 32 KB
 constexpr int kAPitch = 68;                         // floats per A row (68*4 = 272 B)
-constexpr int kATileBytes = kChunk * kAPitch * 4;   // 17408
-constexpr int kATile1Off = kATileBytes + 16;        // second tile shifted by 16 B (other banks)
-constexpr int kAWGBytes = 35840;                    // >= kATile1Off + kATileBytes, multiple of 1024
-constexpr int kStage1Off = 17408;                   // output staging of the second tile (1024-aligned)
-constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
+constexpr int kATileStride = kChunk * kAPitch * 4;  // 17408 = 17 * 1024: A, then X staging
+constexpr int kAWGBytes = kTilesPerWG * kATileStride;
+constexpr int kGWGBytes = 2 * kTilesPerWG * 2 * kChunk * 4;   // [parity][tile][g | v][64]
 constexpr uint32_t kTmemCols = 512;
 
 constexpr int kOffK = 0;
@@ -358,45 +357,49 @@ __device__ __forceinline__ void frag_from_acc(const float (&acc)[2][4], Frag16 &
 // step ks, n8 tile nt and this lane (g = lane / 4, t = lane % 4) the pair
 // (Bm[8ks + 2t][8nt + g], Bm[8ks + 2t + 1][8nt + g]) is the float2 at
 // rowp + (8 nt + g) * kAPitch + 8 ks + 2 t, i.e. Bm is the transpose of the
-// row-major 16x16 block at rowp.  The three split terms accumulate into
-// separate registers (acc.v[0] small*big, [1] big*small, [2] big*big), so the
-// twelve mma.sync of one product form six short independent chains.
-struct Acc3 {
-    float v[3][2][4];
-};
-
-__device__ __forceinline__ void acc3_zero(Acc3 &a) {
+// row-major 16x16 block at rowp.  The twelve mma.sync go to four accumulators
+// (k8 step x n8 tile) in term-major order, so dependent instructions are four
+// apart (longer than the mma.sync latency); the small cross terms come first.
+__device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag16 &f,
+                                                  const float *rowp, int g, int t) {
+    uint32_t bb[2][2][2], bs[2][2][2];   // [ks][nt][pair element]
 #pragma unroll
-    for (int i = 0; i < 3; ++i)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a.v[i][nt][e] = 0.0f;
-}
-
-__device__ __forceinline__ void acc3_sum(const Acc3 &a, float (&out)[2][4]) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) out[nt][e] = a.v[2][nt][e] + (a.v[0][nt][e] + a.v[1][nt][e]);
-}
-
-__device__ __forceinline__ void mma3_times_blockT(Acc3 &acc, const Frag16 &f, const float *rowp,
-                                                  int g, int t) {
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
+    for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const float2 b = *reinterpret_cast<const float2 *>(rowp + (8 * nt + g) * kAPitch +
                                                                8 * ks + 2 * t);
-            uint32_t bb0, bs0, bb1, bs1;
-            split_tf32(b.x, bb0, bs0);
-            split_tf32(b.y, bb1, bs1);
-            mma_tf32(acc.v[0][nt], f.small[ks], bb0, bb1);
-            mma_tf32(acc.v[1][nt], f.big[ks], bs0, bs1);
-            mma_tf32(acc.v[2][nt], f.big[ks], bb0, bb1);
+            split_tf32(b.x, bb[ks][nt][0], bs[ks][nt][0]);
+            split_tf32(b.y, bb[ks][nt][1], bs[ks][nt][1]);
         }
-    }
+    float part[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part[nt][e] = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[nt], f.small[0], bb[0][nt][0], bb[0][nt][1]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) mma_tf32(part[nt], f.small[1], bb[1][nt][0], bb[1][nt][1]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[nt], f.big[0], bs[0][nt][0], bs[0][nt][1]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) mma_tf32(part[nt], f.big[1], bs[1][nt][0], bs[1][nt][1]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[nt], f.big[0], bb[0][nt][0], bb[0][nt][1]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) mma_tf32(part[nt], f.big[1], bb[1][nt][0], bb[1][nt][1]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] += part[nt][e];
+}
+
+__device__ __forceinline__ void zero_acc(float (&a)[2][4]) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[nt][e] = 0.0f;
 }
 
 // Left operand D_JJ^T (= Z_JJ) read from its parking block.
@@ -411,35 +414,68 @@ __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag1
     }
 }
 
-// Blocks Z_JI = X_IJ^T for I = J+1..3 of one tile (At = its A buffer), stored in
-// Z[OFF + I - J - 1].  Split operands are rebuilt when needed instead of cached,
-// to stay within registers.
-template <int J, int OFF>
-__device__ __forceinline__ void merge_column(const float *At, int g, int t, float (&Z)[3][2][4]) {
+// All six off-diagonal blocks of one tile in one warp, as Z_JI = X_IJ^T:
+//   level 1: Z_01, Z_12, Z_23          (one A product each)
+//   level 2: Z_02, Z_13                (two A products each)
+//   level 3: Z_03                      (three A products)
+// each followed by the D_II^T product.  Products of one level are independent,
+// so their mma.sync chains overlap.  z = {Z_01, Z_12, Z_23, Z_02, Z_13, Z_03}.
+// zo = -(acc as left operand) * D_II^T.
+__device__ __forceinline__ void finish_block(const float (&acc)[2][4], const float *At, int I,
+                                             int g, int t, float (&zo)[2][4]) {
+    Frag16 rf;
+    frag_from_acc(acc, rf);
+    float zz[2][4];
+    zero_acc(zz);
+    mma3_times_blockT(zz, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
 #pragma unroll
-    for (int I = J + 1; I < 4; ++I) {
-        Acc3 acc;
-        acc3_zero(acc);
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int M = J; M < I; ++M) {
-            Frag16 f;
-            if (M == J) frag_from_dT(At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J), g, t, f);
-            else frag_from_acc(Z[OFF + M - J - 1], f);
-            mma3_times_blockT(acc, f, At + 16 * I * kAPitch + 16 * M, g, t);
-        }
-        float r[2][4];
-        acc3_sum(acc, r);
-        Frag16 rf;
-        frag_from_acc(r, rf);
-        acc3_zero(acc);
-        mma3_times_blockT(acc, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
-        float z[2][4];
-        acc3_sum(acc, z);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) Z[OFF + I - J - 1][nt][e] = -z[nt][e];
-    }
+        for (int e = 0; e < 4; ++e) zo[nt][e] = -zz[nt][e];
+}
+
+__device__ __forceinline__ const float *dT_block(const float *At, int J) {
+    return At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J);
+}
+
+__device__ __forceinline__ void merge_tile(const float *At, int g, int t, float (&z)[6][2][4]) {
+    auto A = [At](int I, int M) { return At + 16 * I * kAPitch + 16 * M; };
+    Frag16 f;
+    // level 1: Z_01, Z_12, Z_23
+    float a01[2][4], a12[2][4], a23[2][4];
+    zero_acc(a01); zero_acc(a12); zero_acc(a23);
+    frag_from_dT(dT_block(At, 0), g, t, f);
+    mma3_times_blockT(a01, f, A(1, 0), g, t);
+    frag_from_dT(dT_block(At, 1), g, t, f);
+    mma3_times_blockT(a12, f, A(2, 1), g, t);
+    frag_from_dT(dT_block(At, 2), g, t, f);
+    mma3_times_blockT(a23, f, A(3, 2), g, t);
+    finish_block(a01, At, 1, g, t, z[0]);
+    finish_block(a12, At, 2, g, t, z[1]);
+    finish_block(a23, At, 3, g, t, z[2]);
+    // level 2: Z_02 = -(Z_00 A_20^T + Z_01 A_21^T) D_22^T, Z_13 likewise
+    float a02[2][4], a13[2][4];
+    zero_acc(a02); zero_acc(a13);
+    frag_from_dT(dT_block(At, 0), g, t, f);
+    mma3_times_blockT(a02, f, A(2, 0), g, t);
+    frag_from_dT(dT_block(At, 1), g, t, f);
+    mma3_times_blockT(a13, f, A(3, 1), g, t);
+    frag_from_acc(z[0], f);
+    mma3_times_blockT(a02, f, A(2, 1), g, t);
+    frag_from_acc(z[1], f);
+    mma3_times_blockT(a13, f, A(3, 2), g, t);
+    finish_block(a02, At, 2, g, t, z[3]);
+    finish_block(a13, At, 3, g, t, z[4]);
+    // level 3: Z_03 = -(Z_00 A_30^T + Z_01 A_31^T + Z_02 A_32^T) D_33^T
+    float a03[2][4];
+    zero_acc(a03);
+    frag_from_dT(dT_block(At, 0), g, t, f);
+    mma3_times_blockT(a03, f, A(3, 0), g, t);
+    frag_from_acc(z[0], f);
+    mma3_times_blockT(a03, f, A(3, 1), g, t);
+    frag_from_acc(z[3], f);
+    mma3_times_blockT(a03, f, A(3, 2), g, t);
+    finish_block(a03, At, 3, g, t, z[5]);
 }
 
 // ------------------------------------------------------------ output staging
@@ -607,8 +643,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int w = 0; w < kNumWG; ++w) {
-            mbar_init(bar_tfull + 8 * w, 1);
-            mbar_init(bar_tempty + 8 * w, 4);
+            mbar_init(bar_tfull + 8 * w, 2);      // both pairs of a round
+            mbar_init(bar_tempty + 8 * w, 4);     // the warpgroup's four warps
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -668,15 +704,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
+        // Pair q goes to warpgroup w = (q / 2) % kNumWG, TMEM slot q % 2 (128
+        // columns each); the warpgroup's full barrier completes after both
+        // pairs of its round (a round with one pair gets a plain arrive).
         if (lane == 0) {
             int64_t q = 0;
             for (; q < n_local; ++q) {
                 if (*abort_flag) break;
                 const int s = static_cast<int>(q % kNumStages);
                 const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
-                const int w = static_cast<int>(q % kNumWG);
-                const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
-                if (!mbar_wait(bar_full + 8 * s, ph) || !mbar_wait(bar_tempty + 8 * w, phw ^ 1)) {
+                const int64_t round = q >> 1;
+                const int slot = static_cast<int>(q & 1);
+                const int w = static_cast<int>(round % kNumWG);
+                const uint32_t phw = static_cast<uint32_t>((round / kNumWG) & 1);
+                if (!mbar_wait(bar_full + 8 * s, ph) ||
+                    (slot == 0 && !mbar_wait(bar_tempty + 8 * w, phw ^ 1))) {
                     record_timeout(p, abort_flag);
                     break;
                 }
@@ -684,7 +726,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const uint32_t st = sbase + kOffK + s * kStageBytes;
 #pragma unroll
                 for (int bt = 0; bt < 2; ++bt) {
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(256 * w + 128 * slot + 64 * bt);
 #pragma unroll
                     for (int kh = 0; kh < 2; ++kh) {
 #pragma unroll
@@ -698,76 +740,84 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 tc_commit(bar_empty + 8 * s);
                 tc_commit(bar_tfull + 8 * w);
+                if (slot == 0 && q + 1 == n_local) mbar_arrive(bar_tfull + 8 * w);
             }
-            // The last pair's MMAs must be complete before TMEM is released.
+            // The last round's MMAs must be complete before TMEM is released.
             if (q > 0) {
-                const int64_t r = q - 1;
-                const int w = static_cast<int>(r % kNumWG);
-                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
+                const int64_t round = (q - 1) >> 1;
+                const int w = static_cast<int>(round % kNumWG);
+                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((round / kNumWG) & 1)))
                     record_timeout(p, abort_flag);
             }
         }
     } else {
         // ------------------------------------------------ consumer warpgroups
+        // A round = two pairs = four tiles; tile index tix = 2 * slot + tt.
         const int wg = warp >> 2;
         const int qd = warp & 3;                 // TMEM lane quadrant of this warp
-        const int tt_e = qd >> 1;                // epilogue: tile of this thread's row
+        const int tt_e = qd >> 1;                // epilogue: tile (within a pair) of this thread's row
         const int i_e = 32 * (qd & 1) + lane;    // epilogue: row within the tile
-        const int tid = threadIdx.x & 127;       // thread index inside the warpgroup
         const int g8 = lane >> 2, t4 = lane & 3; // mma.sync fragment coordinates
-        uint8_t *abuf = smem + kOffA + wg * kAWGBytes;
-        float *const At0 = reinterpret_cast<float *>(abuf);
-        float *const At1 = reinterpret_cast<float *>(abuf + kATile1Off);
-        auto At = [At0, At1](int t) { return t ? At1 : At0; };
-        float *gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);   // [parity][tile][64]
-        float *vbuf = gbuf + 2 * 2 * kChunk;                                       // [parity][tile][64]
+        uint8_t *const abuf = smem + kOffA + wg * kAWGBytes;
+        float *const gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);
         const int bar_id = 1 + wg;
+        const int64_t n_rounds = (n_local + 1) >> 1;
+        auto pair_tile = [&](int64_t qloc, int tt) -> Tile {
+            if (qloc >= n_local) return Tile{0, 0, 0};
+            return tile_of(p, 2 * (blockIdx.x + qloc * gridDim.x) + tt);
+        };
 
-        int64_t q = wg;
-        RowIn rin = load_row(p, tile_of(p, 2 * (blockIdx.x + q * gridDim.x) + tt_e), i_e);
+        int64_t k = wg;
+        RowIn rin[2];
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl) rin[sl] = load_row(p, pair_tile(2 * k + sl, tt_e), i_e);
 
-        for (int r = 0; q < n_local; ++r, q += kNumWG) {
-            const int64_t pair = blockIdx.x + q * gridDim.x;
-            // Prefetch the next pair's row inputs for this thread's tile.
-            const int64_t qn = q + kNumWG;
-            RowIn rnext;
-            if (qn < n_local) rnext = load_row(p, tile_of(p, 2 * (blockIdx.x + qn * gridDim.x) + tt_e), i_e);
-            else rnext = load_row(p, Tile{0, 0, 0}, i_e);
+        for (int r = 0; k < n_rounds; ++r, k += kNumWG) {
+            // Prefetch the next round's row inputs.
+            RowIn rnext[2];
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl)
+                rnext[sl] = load_row(p, pair_tile(2 * (k + kNumWG) + sl, tt_e), i_e);
 
+            if (lane == 0) bulk_wait_read();   // this warp's last TMA store has read its staging
             if (qd == 0 && lane == 0) {
-                bulk_wait_read();          // last pair's TMA stores have read the staging
                 int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
                 wg_flag[wg] = ok;
             }
-            // Gate factors around the chunk's reference: exp(g_i - g_j) =
-            // u_i * v_j with u_i = exp(g_i - gref), v_j = exp(gref - g_j).  Used
-            // only when every |g - gref| <= 30 in both tiles (no overflow, and
-            // the [-50, 50] clamp cannot bind); otherwise the clamped
-            // exp(g_i - g_j) is evaluated directly.
-            const bool rowok = i_e < tile_of(p, 2 * pair + tt_e).L;
-            float ui = 1.0f, vi = 1.0f;
+            // Gate factors (see the epilogue); g and v of this thread's two rows.
             bool unsafe = false;
-            if (p.g && rowok) {
-                const float d = rin.g - 0.5f * (rin.gfirst + rin.glast);
-                unsafe = !(fabsf(d) <= 30.0f);
-                ui = expf(d);
-                vi = expf(-d);
+            float ui[2];
+            bool rowok[2];
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) {
+                rowok[sl] = i_e < pair_tile(2 * k + sl, tt_e).L;
+                float u = 1.0f, v = 1.0f;
+                if (p.g && rowok[sl]) {
+                    const float d = rin[sl].g - 0.5f * (rin[sl].gfirst + rin[sl].glast);
+                    unsafe |= !(fabsf(d) <= 30.0f);
+                    u = expf(d);
+                    v = expf(-d);
+                }
+                ui[sl] = u;
+                float *gv = gbuf + ((r & 1) * kTilesPerWG + 2 * sl + tt_e) * 2 * kChunk;
+                gv[i_e] = rin[sl].g;
+                gv[kChunk + i_e] = rowok[sl] ? v : 0.0f;
             }
-            float *gcur = gbuf + (r & 1) * 2 * kChunk + tt_e * kChunk;
-            float *vcur = vbuf + (r & 1) * 2 * kChunk + tt_e * kChunk;
-            gcur[i_e] = rin.g;
-            vcur[i_e] = rowok ? vi : 0.0f;
-            const bool direct = named_bar_red_or(bar_id, 128, unsafe);   // B2: g, v ready; A free
+            const bool direct = named_bar_red_or(bar_id, 128, unsafe);   // B2: g, v ready; buffers free
             if (!wg_flag[wg]) break;
             tc_fence_after();
 
-            // ---- epilogue: S row from TMEM -> A row in shared memory
-            {
+            // ---- epilogue: this thread's row of both pairs, TMEM -> A rows (one
+            //      pair at a time; TMEM is released after the second load)
+            // Rows 0..31 only need columns j < 32 (A is strictly lower).
+            const int n4 = (qd & 1) ? 16 : 8;
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) {
                 uint32_t sr[64];
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
-                                       static_cast<uint32_t>(128 * wg + 64 * tt_e);
                 {
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
+                                           static_cast<uint32_t>(256 * wg + 128 * sl + 64 * tt_e);
                     uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
                     uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
                     tmem_ld32(taddr, lo);
@@ -776,23 +826,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 64; ++j) reg_fence(sr[j]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
-
-                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + i_e * kAPitch);
-                // Rows 0..31 only need columns j < 32 (A is strictly lower).
-                const int n4 = (qd & 1) ? 16 : 8;
-                if (!rowok) {
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (sl == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
+                }
+                const int tix = 2 * sl + tt_e;
+                float4 *Arow = reinterpret_cast<float4 *>(abuf + tix * kATileStride) + i_e * (kAPitch / 4);
+                const float *gt = gbuf + ((r & 1) * kTilesPerWG + tix) * 2 * kChunk;
+                const float *vt = gt + kChunk;
+                if (!rowok[sl]) {
 #pragma unroll
-                    for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = z;
+                    for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
                 } else if (!direct) {
-                    const float w = bf16_bits_to_float(rin.beta) * ui;
+                    const float w = bf16_bits_to_float(rin[sl].beta) * ui[sl];
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
-                            const float4 v = reinterpret_cast<const float4 *>(vcur)[j4];
+                            const float4 v = reinterpret_cast<const float4 *>(vt)[j4];
                             float4 a;
                             a.x = (__uint_as_float(sr[4 * j4 + 0]) * w) * v.x;
                             a.y = (__uint_as_float(sr[4 * j4 + 1]) * w) * v.y;
@@ -802,11 +853,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                     }
                 } else {
-                    const float gi = rin.g, bi = bf16_bits_to_float(rin.beta);
+                    const float gi = rin[sl].g, bi = bf16_bits_to_float(rin[sl].beta);
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
-                            const float4 gj = reinterpret_cast<const float4 *>(gcur)[j4];
+                            const float4 gj = reinterpret_cast<const float4 *>(gt)[j4];
                             float4 a;
                             a.x = bi * __uint_as_float(sr[4 * j4 + 0]) *
                                   __expf(fminf(fmaxf(gi - gj.x, -50.f), 50.f));
@@ -821,90 +872,81 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            named_bar_sync(bar_id, 128);                       // B3: A complete
+            named_bar_sync(bar_id, 128);                       // B3: A of all four tiles ready
 
-            // ---- diagonal inverses: thread -> (tile, block I, row c)
-            const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
-            const float4 *dslot = reinterpret_cast<const float4 *>(
-                At(dt) + (16 * dslot_r(dI) + dc) * kAPitch + 16 * dslot_c(dI));
-            {
-                float drow[16];
-                diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
-                float4 *dst = reinterpret_cast<float4 *>(At(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
-                                                         16 * dslot_c(dI));
+            // ---- the rest of the tile belongs to one warp: warp qd -> tile tix = qd
+            const Tile T = pair_tile(2 * k + (qd >> 1), qd & 1);
+            if (T.L > 0) {
+                float *const At = reinterpret_cast<float *>(abuf + qd * kATileStride);
+                uint8_t *const stg = abuf + qd * kATileStride;
+                // Diagonal inverses: pass pp covers blocks 2pp (lanes 0-15) and 2pp+1.
 #pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4)
-                    dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
-            }
-            named_bar_sync(bar_id, 128);                       // B3b: D blocks ready
-
-            // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column)
-            const int mt = qd & 1;
-            float zb[3][2][4];     // Z blocks; see the staging below for their (I, J)
-            if (qd < 2) {
-                merge_column<0, 0>(At(mt), g8, t4, zb);
-            } else {
-                merge_column<1, 0>(At(mt), g8, t4, zb);
-                merge_column<2, 2>(At(mt), g8, t4, zb);
-            }
-            float4 dv[4];
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int I = 2 * pp + (lane >> 4), c = lane & 15;
+                    float drow[16];
+                    diag_inverse_row(At + 16 * I * (kAPitch + 1), c, drow);
+                    float4 *dst = reinterpret_cast<float4 *>(At + (16 * dslot_r(I) + c) * kAPitch +
+                                                             16 * dslot_c(I));
 #pragma unroll
-            for (int m = 0; m < 4; ++m) dv[m] = dslot[m];
-            named_bar_sync(bar_id, 128);                       // B4: A and D no longer read
-
-            // ---- assemble X in the swizzled staging (reuses the A buffer)
-            {
-                uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
-                // zb[k] holds block (I, J): J=0 warps (1,0),(2,0),(3,0); others (2,1),(3,1),(3,2)
-                const int bI0 = qd < 2 ? 1 : 2, bJ0 = qd < 2 ? 0 : 1;
-                const int bI1 = qd < 2 ? 2 : 3, bJ1 = qd < 2 ? 0 : 1;
-                const int bI2 = 3, bJ2 = qd < 2 ? 0 : 2;
-                stage_block_T<OUT_BF16>(st_m, bI0, bJ0, zb[0], g8, t4);
-                stage_block_T<OUT_BF16>(st_m, bI1, bJ1, zb[1], g8, t4);
-                stage_block_T<OUT_BF16>(st_m, bI2, bJ2, zb[2], g8, t4);
-                stage_diag_row<OUT_BF16>(abuf + (dt ? kStage1Off : 0), 16 * dI + dc, dI, dv);
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(bar_id, 128);                       // B5: X complete
-
-            // ---- store: full chunks by TMA from the staging, partial chunks row by row
-            if (tid == 0) {
-                bool any = false;
-#pragma unroll
-                for (int t2 = 0; t2 < 2; ++t2) {
-                    const Tile ts = tile_of(p, 2 * pair + t2);
-                    if (ts.L == kChunk) {
-                        const uint32_t src = smem_u32(abuf + (t2 ? kStage1Off : 0));
-                        tma_store_3d(&tmap_out, src, 0, ts.h, static_cast<int>(ts.row0));
-                        if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, ts.h, static_cast<int>(ts.row0));
-                        any = true;
-                    }
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
                 }
-                if (any) bulk_commit();
-            }
-            {
-                const int st_t = qd >> 1;
-                const Tile ts = tile_of(p, 2 * pair + st_t);
-                if (ts.L > 0 && ts.L < kChunk) {
-                    const uint8_t *sb = abuf + (st_t ? kStage1Off : 0);
+                __syncwarp();
+                float z[6][2][4];   // Z_01, Z_12, Z_23, Z_02, Z_13, Z_03
+                merge_tile(At, g8, t4, z);
+                // This lane's two diagonal-block rows, read before the staging overwrites them.
+                float4 dv[2][4];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int rr = lane + 32 * h2, I = rr >> 4, c = rr & 15;
+                    const float4 *ds = reinterpret_cast<const float4 *>(
+                        At + (16 * dslot_r(I) + c) * kAPitch + 16 * dslot_c(I));
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) dv[h2][m] = ds[m];
+                }
+                __syncwarp();
+                // ---- assemble X in the swizzled staging (reuses this tile's A buffer)
+                stage_block_T<OUT_BF16>(stg, 1, 0, z[0], g8, t4);
+                stage_block_T<OUT_BF16>(stg, 2, 1, z[1], g8, t4);
+                stage_block_T<OUT_BF16>(stg, 3, 2, z[2], g8, t4);
+                stage_block_T<OUT_BF16>(stg, 2, 0, z[3], g8, t4);
+                stage_block_T<OUT_BF16>(stg, 3, 1, z[4], g8, t4);
+                stage_block_T<OUT_BF16>(stg, 3, 0, z[5], g8, t4);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int rr = lane + 32 * h2;
+                    stage_diag_row<OUT_BF16>(stg, rr, rr >> 4, dv[h2]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                // ---- store: a full chunk by TMA, a partial chunk row by row
+                if (T.L == kChunk) {
+                    if (lane == 0) {
+                        const uint32_t src = smem_u32(stg);
+                        tma_store_3d(&tmap_out, src, 0, T.h, static_cast<int>(T.row0));
+                        if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, T.h, static_cast<int>(T.row0));
+                        bulk_commit();
+                    }
+                } else {
                     constexpr int kPieces = OUT_BF16 ? 8 : 16;
                     constexpr int kRowsPerIt = 32 / kPieces;
 #pragma unroll 2
-                    for (int it = 0; it < 32 / kRowsPerIt; ++it) {
-                        const int rr = 32 * (qd & 1) + kRowsPerIt * it + lane / kPieces;
+                    for (int it = 0; it < 64 / kRowsPerIt; ++it) {
+                        const int rr = kRowsPerIt * it + lane / kPieces;
                         const int piece = lane % kPieces;
-                        if (rr < ts.L) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(sb + stage_piece_off<OUT_BF16>(rr, piece));
-                            const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
+                        if (rr < T.L) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(stg + stage_piece_off<OUT_BF16>(rr, piece));
+                            const int64_t orow = (T.row0 + rr) * p.H + T.h;
                             *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
                                                        orow * (OUT_BF16 ? 128 : 256) + 16 * piece) = v;
                         }
                     }
                 }
             }
-            rin = rnext;
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) rin[sl] = rnext[sl];
         }
-        if (tid == 0) bulk_wait_all();
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
