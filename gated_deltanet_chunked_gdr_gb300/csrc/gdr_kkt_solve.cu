@@ -46,9 +46,8 @@ namespace gdr {
 
 constexpr int kChunk = 64;
 constexpr int kHeadK = 128;
-constexpr int kNumWG = 2;
-constexpr int kNumStages = 2;
-constexpr int kTilesPerWG = 4;                      // two MMA pairs per warpgroup round
+constexpr int kNumWG = 3;
+constexpr int kNumStages = 3;
 constexpr int kNumConsumerWarps = 4 * kNumWG;
 constexpr int kProducerWarp = kNumConsumerWarps;
 constexpr int kMmaWarp = kNumConsumerWarps + 1;
@@ -57,9 +56,10 @@ constexpr int kNumThreads = (kNumConsumerWarps + 2) * 32;
 constexpr int kBoxBytes = kChunk * 64 * 2;          // one (tile, K-half) box: 64 rows x 128 B
 constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][128 B] = 32 KB
 constexpr int kAPitch = 68;                         // floats per A row (68*4 = 272 B)
-constexpr int kATileStride = kChunk * kAPitch * 4;  // 17408 = 17 * 1024: A, then X staging
-constexpr int kAWGBytes = kTilesPerWG * kATileStride;
-constexpr int kGWGBytes = 2 * kTilesPerWG * 2 * kChunk * 4;   // [parity][tile][g | v][64]
+constexpr int kATileBytes = kChunk * kAPitch * 4;   // 17408
+constexpr int kATile1Off = kATileBytes + 16;        // second tile shifted by 16 B (other banks)
+constexpr int kAWGBytes = 34944;                    // >= kATile1Off + kATileBytes, multiple of 128
+constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
 constexpr uint32_t kTmemCols = 512;
 
 constexpr int kOffK = 0;
@@ -395,13 +395,6 @@ __device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag
         for (int e = 0; e < 4; ++e) acc[nt][e] += part[nt][e];
 }
 
-__device__ __forceinline__ void zero_acc(float (&a)[2][4]) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) a[nt][e] = 0.0f;
-}
-
 // Left operand D_JJ^T (= Z_JJ) read from its parking block.
 __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag16 &f) {
 #pragma unroll
@@ -414,151 +407,44 @@ __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag1
     }
 }
 
-// All six off-diagonal blocks of one tile in one warp, as Z_JI = X_IJ^T:
-//   level 1: Z_01, Z_12, Z_23          (one A product each)
-//   level 2: Z_02, Z_13                (two A products each)
-//   level 3: Z_03                      (three A products)
-// each followed by the D_II^T product.  Products of one level are independent,
-// so their mma.sync chains overlap.  z = {Z_01, Z_12, Z_23, Z_02, Z_13, Z_03}.
-// zo = -(acc as left operand) * D_II^T.
-__device__ __forceinline__ void finish_block(const float (&acc)[2][4], const float *At, int I,
-                                             int g, int t, float (&zo)[2][4]) {
-    Frag16 rf;
-    frag_from_acc(acc, rf);
-    float zz[2][4];
-    zero_acc(zz);
-    mma3_times_blockT(zz, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
+// Blocks Z_JI = X_IJ^T for I = J+1..3 of one tile (At = its A buffer).  Split
+// operands are rebuilt when needed instead of cached, to stay within registers.
+template <int J>
+__device__ __forceinline__ void merge_column(const float *At, int g, int t,
+                                             float (&Z)[3 - J][2][4]) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int I = J + 1; I < 4; ++I) {
+        float acc[2][4] = {};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) zo[nt][e] = -zz[nt][e];
-}
-
-__device__ __forceinline__ const float *dT_block(const float *At, int J) {
-    return At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J);
-}
-
-__device__ __forceinline__ void merge_tile(const float *At, int g, int t, float (&z)[6][2][4]) {
-    auto A = [At](int I, int M) { return At + 16 * I * kAPitch + 16 * M; };
-    Frag16 f;
-    // level 1: Z_01, Z_12, Z_23
-    float a01[2][4], a12[2][4], a23[2][4];
-    zero_acc(a01); zero_acc(a12); zero_acc(a23);
-    frag_from_dT(dT_block(At, 0), g, t, f);
-    mma3_times_blockT(a01, f, A(1, 0), g, t);
-    frag_from_dT(dT_block(At, 1), g, t, f);
-    mma3_times_blockT(a12, f, A(2, 1), g, t);
-    frag_from_dT(dT_block(At, 2), g, t, f);
-    mma3_times_blockT(a23, f, A(3, 2), g, t);
-    finish_block(a01, At, 1, g, t, z[0]);
-    finish_block(a12, At, 2, g, t, z[1]);
-    finish_block(a23, At, 3, g, t, z[2]);
-    // level 2: Z_02 = -(Z_00 A_20^T + Z_01 A_21^T) D_22^T, Z_13 likewise
-    float a02[2][4], a13[2][4];
-    zero_acc(a02); zero_acc(a13);
-    frag_from_dT(dT_block(At, 0), g, t, f);
-    mma3_times_blockT(a02, f, A(2, 0), g, t);
-    frag_from_dT(dT_block(At, 1), g, t, f);
-    mma3_times_blockT(a13, f, A(3, 1), g, t);
-    frag_from_acc(z[0], f);
-    mma3_times_blockT(a02, f, A(2, 1), g, t);
-    frag_from_acc(z[1], f);
-    mma3_times_blockT(a13, f, A(3, 2), g, t);
-    finish_block(a02, At, 2, g, t, z[3]);
-    finish_block(a13, At, 3, g, t, z[4]);
-    // level 3: Z_03 = -(Z_00 A_30^T + Z_01 A_31^T + Z_02 A_32^T) D_33^T
-    float a03[2][4];
-    zero_acc(a03);
-    frag_from_dT(dT_block(At, 0), g, t, f);
-    mma3_times_blockT(a03, f, A(3, 0), g, t);
-    frag_from_acc(z[0], f);
-    mma3_times_blockT(a03, f, A(3, 1), g, t);
-    frag_from_acc(z[3], f);
-    mma3_times_blockT(a03, f, A(3, 2), g, t);
-    finish_block(a03, At, 3, g, t, z[5]);
-}
-
-// ------------------------------------------------------------ output staging
-// X is assembled in the layout a 128-byte-swizzled TMA store reads: a tile's 64
-// rows of 128 bytes (bf16: 64 values; fp32: two 32-value halves 8 KB apart), the
-// 16-byte piece q of row r stored at piece position q ^ (r % 8).
-template <bool BF16>
-__device__ __forceinline__ uint32_t stage_piece_off(int r, int q) {
-    if (BF16) return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
-    return static_cast<uint32_t>((q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4));
-}
-
-template <bool BF16>
-__device__ __forceinline__ void stage_put(uint8_t *st, int r, int c, float v) {
-    if (BF16) {
-        *reinterpret_cast<__nv_bfloat16 *>(st + stage_piece_off<true>(r, c >> 3) + 2 * (c & 7)) =
-            __float2bfloat16_rn(v);
-    } else {
-        *reinterpret_cast<float *>(st + stage_piece_off<false>(r, c >> 2) + 4 * (c & 3)) = v;
+        for (int M = J; M < I; ++M) {
+            Frag16 f;
+            if (M == J) frag_from_dT(At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J), g, t, f);
+            else frag_from_acc(Z[M - J - 1], f);
+            mma3_times_blockT(acc, f, At + 16 * I * kAPitch + 16 * M, g, t);
+        }
+        Frag16 rf;
+        frag_from_acc(acc, rf);
+        float z[2][4] = {};
+        mma3_times_blockT(z, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Z[I - J - 1][nt][e] = -z[nt][e];
     }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// Row r of X restricted to columns >= 16 I: the diagonal block row (d[0..3] =
-// 16 values) followed by zeros.
-template <bool BF16>
-__device__ __forceinline__ void stage_diag_row(uint8_t *st, int r, int I, const float4 (&d)[4]) {
-    if (BF16) {
-        uint4 a, b;
-        a.x = pack_bf16x2(d[0].x, d[0].y); a.y = pack_bf16x2(d[0].z, d[0].w);
-        a.z = pack_bf16x2(d[1].x, d[1].y); a.w = pack_bf16x2(d[1].z, d[1].w);
-        b.x = pack_bf16x2(d[2].x, d[2].y); b.y = pack_bf16x2(d[2].z, d[2].w);
-        b.z = pack_bf16x2(d[3].x, d[3].y); b.w = pack_bf16x2(d[3].z, d[3].w);
-        *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I)) = a;
-        *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I + 1)) = b;
-#pragma unroll
-        for (int q = 2; q < 8; ++q)
-            if (q >= 2 * I + 2) *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, q)) = make_uint4(0, 0, 0, 0);
-    } else {
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            *reinterpret_cast<float4 *>(st + stage_piece_off<false>(r, 4 * I + m)) = d[m];
-#pragma unroll
-        for (int q = 4; q < 16; ++q)
-            if (q >= 4 * I + 4)
-                *reinterpret_cast<float4 *>(st + stage_piece_off<false>(r, q)) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-}
-
-// Z_JI (accumulator layout) -> rows 16I.. / columns 16J.. of X in the staging.
-template <bool BF16>
-__device__ __forceinline__ void stage_block_T(uint8_t *st, int I, int J, const float (&z)[2][4],
+// Writes Z_JI (accumulator layout) into rows 16I.. / columns 16J.. of X.
+__device__ __forceinline__ void store_block_T(float *At, int I, int J, const float (&z)[2][4],
                                               int g, int t) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        const int r0 = 16 * I + 8 * nt + 2 * t, c0 = 16 * J + g;
-        stage_put<BF16>(st, r0, c0, z[nt][0]);
-        stage_put<BF16>(st, r0 + 1, c0, z[nt][1]);
-        stage_put<BF16>(st, r0, c0 + 8, z[nt][2]);
-        stage_put<BF16>(st, r0 + 1, c0 + 8, z[nt][3]);
+        float *r0 = At + (16 * I + 8 * nt + 2 * t) * kAPitch + 16 * J + g;
+        r0[0] = z[nt][0];
+        r0[kAPitch] = z[nt][1];
+        r0[8] = z[nt][2];
+        r0[kAPitch + 8] = z[nt][3];
     }
 }
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y), "r"(z), "r"(src)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 
 __device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag) {
     *abort_flag = 1;
@@ -620,8 +506,7 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
 
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(kNumThreads, 1)
-    kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_out, const Params p) {
+    kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -643,8 +528,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int w = 0; w < kNumWG; ++w) {
-            mbar_init(bar_tfull + 8 * w, 2);      // both pairs of a round
-            mbar_init(bar_tempty + 8 * w, 4);     // the warpgroup's four warps
+            mbar_init(bar_tfull + 8 * w, 1);
+            mbar_init(bar_tempty + 8 * w, 4);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -704,21 +589,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        // Pair q goes to warpgroup w = (q / 2) % kNumWG, TMEM slot q % 2 (128
-        // columns each); the warpgroup's full barrier completes after both
-        // pairs of its round (a round with one pair gets a plain arrive).
         if (lane == 0) {
             int64_t q = 0;
             for (; q < n_local; ++q) {
                 if (*abort_flag) break;
                 const int s = static_cast<int>(q % kNumStages);
                 const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
-                const int64_t round = q >> 1;
-                const int slot = static_cast<int>(q & 1);
-                const int w = static_cast<int>(round % kNumWG);
-                const uint32_t phw = static_cast<uint32_t>((round / kNumWG) & 1);
-                if (!mbar_wait(bar_full + 8 * s, ph) ||
-                    (slot == 0 && !mbar_wait(bar_tempty + 8 * w, phw ^ 1))) {
+                const int w = static_cast<int>(q % kNumWG);
+                const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
+                if (!mbar_wait(bar_full + 8 * s, ph) || !mbar_wait(bar_tempty + 8 * w, phw ^ 1)) {
                     record_timeout(p, abort_flag);
                     break;
                 }
@@ -726,7 +605,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const uint32_t st = sbase + kOffK + s * kStageBytes;
 #pragma unroll
                 for (int bt = 0; bt < 2; ++bt) {
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(256 * w + 128 * slot + 64 * bt);
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
 #pragma unroll
                     for (int kh = 0; kh < 2; ++kh) {
 #pragma unroll
@@ -740,84 +619,83 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 tc_commit(bar_empty + 8 * s);
                 tc_commit(bar_tfull + 8 * w);
-                if (slot == 0 && q + 1 == n_local) mbar_arrive(bar_tfull + 8 * w);
             }
-            // The last round's MMAs must be complete before TMEM is released.
+            // The last pair's MMAs must be complete before TMEM is released.
             if (q > 0) {
-                const int64_t round = (q - 1) >> 1;
-                const int w = static_cast<int>(round % kNumWG);
-                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((round / kNumWG) & 1)))
+                const int64_t r = q - 1;
+                const int w = static_cast<int>(r % kNumWG);
+                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
                     record_timeout(p, abort_flag);
             }
         }
     } else {
         // ------------------------------------------------ consumer warpgroups
-        // A round = two pairs = four tiles; tile index tix = 2 * slot + tt.
         const int wg = warp >> 2;
         const int qd = warp & 3;                 // TMEM lane quadrant of this warp
-        const int tt_e = qd >> 1;                // epilogue: tile (within a pair) of this thread's row
+        const int tt_e = qd >> 1;                // epilogue: tile of this thread's row
         const int i_e = 32 * (qd & 1) + lane;    // epilogue: row within the tile
+        const int tid = threadIdx.x & 127;       // thread index inside the warpgroup
         const int g8 = lane >> 2, t4 = lane & 3; // mma.sync fragment coordinates
-        uint8_t *const abuf = smem + kOffA + wg * kAWGBytes;
-        float *const gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);
+        uint8_t *abuf = smem + kOffA + wg * kAWGBytes;
+        float *const At0 = reinterpret_cast<float *>(abuf);
+        float *const At1 = reinterpret_cast<float *>(abuf + kATile1Off);
+        auto At = [At0, At1](int t) { return t ? At1 : At0; };
+        float *gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);   // [parity][tile][64]
+        float *vbuf = gbuf + 2 * 2 * kChunk;                                       // [parity][tile][64]
         const int bar_id = 1 + wg;
-        const int64_t n_rounds = (n_local + 1) >> 1;
-        auto pair_tile = [&](int64_t qloc, int tt) -> Tile {
-            if (qloc >= n_local) return Tile{0, 0, 0};
-            return tile_of(p, 2 * (blockIdx.x + qloc * gridDim.x) + tt);
-        };
 
-        int64_t k = wg;
-        RowIn rin[2];
-#pragma unroll
-        for (int sl = 0; sl < 2; ++sl) rin[sl] = load_row(p, pair_tile(2 * k + sl, tt_e), i_e);
+        int64_t q = wg;
+        Tile cur0 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x));
+        Tile cur1 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x) + 1);
+        RowIn rin = load_row(p, pick(cur0, cur1, tt_e), i_e);
 
-        for (int r = 0; k < n_rounds; ++r, k += kNumWG) {
-            // Prefetch the next round's row inputs.
-            RowIn rnext[2];
-#pragma unroll
-            for (int sl = 0; sl < 2; ++sl)
-                rnext[sl] = load_row(p, pair_tile(2 * (k + kNumWG) + sl, tt_e), i_e);
+        for (int r = 0; q < n_local; ++r, q += kNumWG) {
+            // Prefetch the next pair's schedule and row inputs.
+            const int64_t qn = q + kNumWG;
+            Tile nx0, nx1;
+            nx0.L = nx1.L = 0;
+            nx0.row0 = nx1.row0 = 0;
+            nx0.h = nx1.h = 0;
+            if (qn < n_local) {
+                nx0 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x));
+                nx1 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x) + 1);
+            }
+            const RowIn rnext = load_row(p, pick(nx0, nx1, tt_e), i_e);
 
-            if (lane == 0) bulk_wait_read();   // this warp's last TMA store has read its staging
             if (qd == 0 && lane == 0) {
                 int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
                 wg_flag[wg] = ok;
             }
-            // Gate factors (see the epilogue); g and v of this thread's two rows.
+            // Gate factors around the chunk's reference: exp(g_i - g_j) =
+            // u_i * v_j with u_i = exp(g_i - gref), v_j = exp(gref - g_j).  Used
+            // only when every |g - gref| <= 30 in both tiles (no overflow, and
+            // the [-50, 50] clamp cannot bind); otherwise the clamped
+            // exp(g_i - g_j) is evaluated directly.
+            const Tile te = pick(cur0, cur1, tt_e);
+            const bool rowok = i_e < te.L;
+            float ui = 1.0f, vi = 1.0f;
             bool unsafe = false;
-            float ui[2];
-            bool rowok[2];
-#pragma unroll
-            for (int sl = 0; sl < 2; ++sl) {
-                rowok[sl] = i_e < pair_tile(2 * k + sl, tt_e).L;
-                float u = 1.0f, v = 1.0f;
-                if (p.g && rowok[sl]) {
-                    const float d = rin[sl].g - 0.5f * (rin[sl].gfirst + rin[sl].glast);
-                    unsafe |= !(fabsf(d) <= 30.0f);
-                    u = expf(d);
-                    v = expf(-d);
-                }
-                ui[sl] = u;
-                float *gv = gbuf + ((r & 1) * kTilesPerWG + 2 * sl + tt_e) * 2 * kChunk;
-                gv[i_e] = rin[sl].g;
-                gv[kChunk + i_e] = rowok[sl] ? v : 0.0f;
+            if (p.g && rowok) {
+                const float d = rin.g - 0.5f * (rin.gfirst + rin.glast);
+                unsafe = !(fabsf(d) <= 30.0f);
+                ui = expf(d);
+                vi = expf(-d);
             }
-            const bool direct = named_bar_red_or(bar_id, 128, unsafe);   // B2: g, v ready; buffers free
+            float *gcur = gbuf + (r & 1) * 2 * kChunk + tt_e * kChunk;
+            float *vcur = vbuf + (r & 1) * 2 * kChunk + tt_e * kChunk;
+            gcur[i_e] = rin.g;
+            vcur[i_e] = rowok ? vi : 0.0f;
+            const bool direct = named_bar_red_or(bar_id, 128, unsafe);   // B2: g, v ready; A free
             if (!wg_flag[wg]) break;
             tc_fence_after();
 
-            // ---- epilogue: this thread's row of both pairs, TMEM -> A rows (one
-            //      pair at a time; TMEM is released after the second load)
-            // Rows 0..31 only need columns j < 32 (A is strictly lower).
-            const int n4 = (qd & 1) ? 16 : 8;
-#pragma unroll
-            for (int sl = 0; sl < 2; ++sl) {
+            // ---- epilogue: S row from TMEM -> A row in shared memory
+            {
                 uint32_t sr[64];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
+                                       static_cast<uint32_t>(128 * wg + 64 * tt_e);
                 {
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
-                                           static_cast<uint32_t>(256 * wg + 128 * sl + 64 * tt_e);
                     uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
                     uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
                     tmem_ld32(taddr, lo);
@@ -826,24 +704,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 64; ++j) reg_fence(sr[j]);
-                if (sl == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
-                }
-                const int tix = 2 * sl + tt_e;
-                float4 *Arow = reinterpret_cast<float4 *>(abuf + tix * kATileStride) + i_e * (kAPitch / 4);
-                const float *gt = gbuf + ((r & 1) * kTilesPerWG + tix) * 2 * kChunk;
-                const float *vt = gt + kChunk;
-                if (!rowok[sl]) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
+
+                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + i_e * kAPitch);
+                // Rows 0..31 only need columns j < 32 (A is strictly lower).
+                const int n4 = (qd & 1) ? 16 : 8;
+                if (!rowok) {
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = z;
                 } else if (!direct) {
-                    const float w = bf16_bits_to_float(rin[sl].beta) * ui[sl];
+                    const float w = bf16_bits_to_float(rin.beta) * ui;
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
-                            const float4 v = reinterpret_cast<const float4 *>(vt)[j4];
+                            const float4 v = reinterpret_cast<const float4 *>(vcur)[j4];
                             float4 a;
                             a.x = (__uint_as_float(sr[4 * j4 + 0]) * w) * v.x;
                             a.y = (__uint_as_float(sr[4 * j4 + 1]) * w) * v.y;
@@ -853,11 +730,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                     }
                 } else {
-                    const float gi = rin[sl].g, bi = bf16_bits_to_float(rin[sl].beta);
+                    const float gi = rin.g, bi = bf16_bits_to_float(rin.beta);
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
-                            const float4 gj = reinterpret_cast<const float4 *>(gt)[j4];
+                            const float4 gj = reinterpret_cast<const float4 *>(gcur)[j4];
                             float4 a;
                             a.x = bi * __uint_as_float(sr[4 * j4 + 0]) *
                                   __expf(fminf(fmaxf(gi - gj.x, -50.f), 50.f));
@@ -872,81 +749,98 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            named_bar_sync(bar_id, 128);                       // B3: A of all four tiles ready
+            named_bar_sync(bar_id, 128);                       // B3: A complete
 
-            // ---- the rest of the tile belongs to one warp: warp qd -> tile tix = qd
-            const Tile T = pair_tile(2 * k + (qd >> 1), qd & 1);
-            if (T.L > 0) {
-                float *const At = reinterpret_cast<float *>(abuf + qd * kATileStride);
-                uint8_t *const stg = abuf + qd * kATileStride;
-                // Diagonal inverses: pass pp covers blocks 2pp (lanes 0-15) and 2pp+1.
+            // ---- diagonal inverses: thread -> (tile, block I, row c)
+            const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
+            float drow[16];
+            diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
+            {
+                float4 *dst = reinterpret_cast<float4 *>(At(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
+                                                         16 * dslot_c(dI));
 #pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    const int I = 2 * pp + (lane >> 4), c = lane & 15;
-                    float drow[16];
-                    diag_inverse_row(At + 16 * I * (kAPitch + 1), c, drow);
-                    float4 *dst = reinterpret_cast<float4 *>(At + (16 * dslot_r(I) + c) * kAPitch +
-                                                             16 * dslot_c(I));
+                for (int j4 = 0; j4 < 4; ++j4)
+                    dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
+            }
+            named_bar_sync(bar_id, 128);                       // B3b: D blocks ready
+
+            // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column);
+            //      then X rows are assembled in the A buffer (after B4 in both branches)
+            const int mt = qd & 1;
+            if (qd < 2) {
+                float z0[3][2][4];
+                merge_column<0>(At(mt), g8, t4, z0);
+                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
+                store_block_T(At(mt), 1, 0, z0[0], g8, t4);
+                store_block_T(At(mt), 2, 0, z0[1], g8, t4);
+                store_block_T(At(mt), 3, 0, z0[2], g8, t4);
+            } else {
+                float z1[2][2][4], z2[1][2][4];
+                merge_column<1>(At(mt), g8, t4, z1);
+                merge_column<2>(At(mt), g8, t4, z2);
+                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
+                store_block_T(At(mt), 2, 1, z1[0], g8, t4);
+                store_block_T(At(mt), 3, 1, z1[1], g8, t4);
+                store_block_T(At(mt), 3, 2, z2[0], g8, t4);
+            }
+            {
+                float4 *row = reinterpret_cast<float4 *>(At(dt) + (16 * dI + dc) * kAPitch);
+                row[4 * dI + 0] = make_float4(drow[0], drow[1], drow[2], drow[3]);
+                row[4 * dI + 1] = make_float4(drow[4], drow[5], drow[6], drow[7]);
+                row[4 * dI + 2] = make_float4(drow[8], drow[9], drow[10], drow[11]);
+                row[4 * dI + 3] = make_float4(drow[12], drow[13], drow[14], drow[15]);
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4)
-                        dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
-                }
-                __syncwarp();
-                float z[6][2][4];   // Z_01, Z_12, Z_23, Z_02, Z_13, Z_03
-                merge_tile(At, g8, t4, z);
-                // This lane's two diagonal-block rows, read before the staging overwrites them.
-                float4 dv[2][4];
+                for (int j4 = 4; j4 < 16; ++j4)
+                    if (j4 >= 4 * dI + 4) row[j4] = z;
+            }
+            named_bar_sync(bar_id, 128);                       // B5: X complete
+
+            // ---- coalesced 16-byte stores: warp -> 32 rows of one tile
+            {
+                const int st_t = qd >> 1;
+                const Tile ts = pick(cur0, cur1, st_t);
+                const float *Xs = At(st_t);
+                if (OUT_BF16) {
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int rr = lane + 32 * h2, I = rr >> 4, c = rr & 15;
-                    const float4 *ds = reinterpret_cast<const float4 *>(
-                        At + (16 * dslot_r(I) + c) * kAPitch + 16 * dslot_c(I));
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) dv[h2][m] = ds[m];
-                }
-                __syncwarp();
-                // ---- assemble X in the swizzled staging (reuses this tile's A buffer)
-                stage_block_T<OUT_BF16>(stg, 1, 0, z[0], g8, t4);
-                stage_block_T<OUT_BF16>(stg, 2, 1, z[1], g8, t4);
-                stage_block_T<OUT_BF16>(stg, 3, 2, z[2], g8, t4);
-                stage_block_T<OUT_BF16>(stg, 2, 0, z[3], g8, t4);
-                stage_block_T<OUT_BF16>(stg, 3, 1, z[4], g8, t4);
-                stage_block_T<OUT_BF16>(stg, 3, 0, z[5], g8, t4);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int rr = lane + 32 * h2;
-                    stage_diag_row<OUT_BF16>(stg, rr, rr >> 4, dv[h2]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                // ---- store: a full chunk by TMA, a partial chunk row by row
-                if (T.L == kChunk) {
-                    if (lane == 0) {
-                        const uint32_t src = smem_u32(stg);
-                        tma_store_3d(&tmap_out, src, 0, T.h, static_cast<int>(T.row0));
-                        if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, T.h, static_cast<int>(T.row0));
-                        bulk_commit();
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = 32 * (qd & 1) + 4 * it + (lane >> 3);
+                        const int piece = lane & 7;
+                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece);
+                        const float4 b = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece + 4);
+                        if (rr < ts.L) {
+                            __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y);
+                            __nv_bfloat162 h1 = __floats2bfloat162_rn(a.z, a.w);
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y);
+                            __nv_bfloat162 h3 = __floats2bfloat162_rn(b.z, b.w);
+                            uint4 v;
+                            v.x = *reinterpret_cast<uint32_t *>(&h0);
+                            v.y = *reinterpret_cast<uint32_t *>(&h1);
+                            v.z = *reinterpret_cast<uint32_t *>(&h2);
+                            v.w = *reinterpret_cast<uint32_t *>(&h3);
+                            const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 128 +
+                                                       16 * piece) = v;
+                        }
                     }
                 } else {
-                    constexpr int kPieces = OUT_BF16 ? 8 : 16;
-                    constexpr int kRowsPerIt = 32 / kPieces;
-#pragma unroll 2
-                    for (int it = 0; it < 64 / kRowsPerIt; ++it) {
-                        const int rr = kRowsPerIt * it + lane / kPieces;
-                        const int piece = lane % kPieces;
-                        if (rr < T.L) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(stg + stage_piece_off<OUT_BF16>(rr, piece));
-                            const int64_t orow = (T.row0 + rr) * p.H + T.h;
-                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
-                                                       orow * (OUT_BF16 ? 128 : 256) + 16 * piece) = v;
+#pragma unroll
+                    for (int it = 0; it < 16; ++it) {
+                        const int rr = 32 * (qd & 1) + 2 * it + (lane >> 4);
+                        const int piece = lane & 15;
+                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 4 * piece);
+                        if (rr < ts.L) {
+                            const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
+                            *reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 256 +
+                                                        16 * piece) = a;
                         }
                     }
                 }
             }
-#pragma unroll
-            for (int sl = 0; sl < 2; ++sl) rin[sl] = rnext[sl];
+            cur0 = nx0;
+            cur1 = nx1;
+            rin = rnext;
         }
-        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -1067,19 +961,6 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GDR_ERR_CUDA;
 
-    CUtensorMap tmap_o;
-    {
-        const int esz = out_dtype == GDR_BF16 ? 2 : 4;
-        const cuuint64_t odims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(ntok)};
-        const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(64 * esz), static_cast<cuuint64_t>(H * 64 * esz)};
-        const cuuint32_t obox[3] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(kChunk)};
-        if (encode(&tmap_o, out_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                   3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return GDR_ERR_CUDA;
-    }
-
     Params prm;
     prm.g = g;
     prm.beta = static_cast<const __nv_bfloat16 *>(beta);
@@ -1104,9 +985,9 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
     const int64_t grid = prm.n_pairs < sms ? prm.n_pairs : sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (out_dtype == GDR_BF16)
-        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
+        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
     else
-        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
+        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }
