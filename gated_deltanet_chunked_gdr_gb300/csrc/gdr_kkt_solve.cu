@@ -547,84 +547,121 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
                                 : 0;
 
+    // Warpgroup w owns pipeline stage w and TMEM columns [128 w, 128 w + 128) and
+    // processes the CTA-local pairs q = w, w + kNumWG, ...  The producer and the
+    // MMA issuer serve the warpgroups round-robin with non-blocking polls, so a
+    // slow warpgroup never holds up the others; each gives up after kWaitNs
+    // without progress.
+    static_assert(kNumStages == kNumWG, "one stage per warpgroup");
     if (warp == kProducerWarp) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
                          : "memory");
-            int64_t q = 0;
-            for (; q < n_local; ++q) {
-                if (*abort_flag) break;
-                const int s = static_cast<int>(q % kNumStages);
-                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
-                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+            int64_t done[kNumWG];
+#pragma unroll
+            for (int w = 0; w < kNumWG; ++w) done[w] = 0;
+            uint64_t t_last = global_timer();
+            while (!*abort_flag) {
+                bool pending = false, progress = false;
+#pragma unroll
+                for (int w = 0; w < kNumWG; ++w) {
+                    const int64_t q = w + kNumWG * done[w];
+                    if (q >= n_local) continue;
+                    pending = true;
+                    const uint32_t ph = static_cast<uint32_t>(done[w] & 1);
+                    if (!mbar_try_wait(bar_empty + 8 * w, ph ^ 1)) continue;
+                    const int64_t pair = blockIdx.x + q * gridDim.x;
+                    const Tile t0 = tile_of(p, 2 * pair);
+                    const Tile t1 = tile_of(p, 2 * pair + 1);
+                    const uint32_t bytes = (t0.L > 0 ? 2 * kBoxBytes : 0) + (t1.L > 0 ? 2 * kBoxBytes : 0);
+                    const uint32_t st = sbase + kOffK + w * kStageBytes;
+                    mbar_arrive_expect_tx(bar_full + 8 * w, bytes);
+                    if (t0.L > 0) {
+                        tma_load_3d(st + 0 * kBoxBytes, &tmap_k, bar_full + 8 * w, 0, t0.h,
+                                    static_cast<int>(t0.row0));
+                        tma_load_3d(st + 2 * kBoxBytes, &tmap_k, bar_full + 8 * w, 64, t0.h,
+                                    static_cast<int>(t0.row0));
+                    }
+                    if (t1.L > 0) {
+                        tma_load_3d(st + 1 * kBoxBytes, &tmap_k, bar_full + 8 * w, 0, t1.h,
+                                    static_cast<int>(t1.row0));
+                        tma_load_3d(st + 3 * kBoxBytes, &tmap_k, bar_full + 8 * w, 64, t1.h,
+                                    static_cast<int>(t1.row0));
+                    }
+                    ++done[w];
+                    progress = true;
+                }
+                if (!pending) break;
+                if (progress) {
+                    t_last = global_timer();
+                } else if (global_timer() - t_last > kWaitNs) {
                     record_timeout(p, abort_flag);
                     break;
-                }
-                const int64_t pair = blockIdx.x + q * gridDim.x;
-                const Tile t0 = tile_of(p, 2 * pair);
-                const Tile t1 = tile_of(p, 2 * pair + 1);
-                const uint32_t bytes = (t0.L > 0 ? 2 * kBoxBytes : 0) + (t1.L > 0 ? 2 * kBoxBytes : 0);
-                const uint32_t st = sbase + kOffK + s * kStageBytes;
-                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
-                if (t0.L > 0) {
-                    tma_load_3d(st + 0 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t0.h,
-                                static_cast<int>(t0.row0));
-                    tma_load_3d(st + 2 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t0.h,
-                                static_cast<int>(t0.row0));
-                }
-                if (t1.L > 0) {
-                    tma_load_3d(st + 1 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t1.h,
-                                static_cast<int>(t1.row0));
-                    tma_load_3d(st + 3 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t1.h,
-                                static_cast<int>(t1.row0));
+                } else {
+                    __nanosleep(20);
                 }
             }
             // Drain: every issued load has landed and every stage's MMAs committed.
-            const int64_t first = q > kNumStages ? q - kNumStages : 0;
-            for (int64_t r = first; r < q; ++r) {
-                const int s = static_cast<int>(r % kNumStages);
-                const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
-                if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
-                if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
+#pragma unroll
+            for (int w = 0; w < kNumWG; ++w) {
+                if (done[w] == 0) continue;
+                const uint32_t ph = static_cast<uint32_t>((done[w] - 1) & 1);
+                if (!mbar_wait(bar_full + 8 * w, ph)) record_timeout(p, abort_flag);
+                if (!mbar_wait(bar_empty + 8 * w, ph)) record_timeout(p, abort_flag);
             }
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            int64_t q = 0;
-            for (; q < n_local; ++q) {
-                if (*abort_flag) break;
-                const int s = static_cast<int>(q % kNumStages);
-                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
-                const int w = static_cast<int>(q % kNumWG);
-                const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
-                if (!mbar_wait(bar_full + 8 * s, ph) || !mbar_wait(bar_tempty + 8 * w, phw ^ 1)) {
-                    record_timeout(p, abort_flag);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t st = sbase + kOffK + s * kStageBytes;
+            int64_t done[kNumWG];
 #pragma unroll
-                for (int bt = 0; bt < 2; ++bt) {
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
+            for (int w = 0; w < kNumWG; ++w) done[w] = 0;
+            uint64_t t_last = global_timer();
+            while (!*abort_flag) {
+                bool pending = false, progress = false;
 #pragma unroll
-                    for (int kh = 0; kh < 2; ++kh) {
+                for (int w = 0; w < kNumWG; ++w) {
+                    const int64_t q = w + kNumWG * done[w];
+                    if (q >= n_local) continue;
+                    pending = true;
+                    const uint32_t ph = static_cast<uint32_t>(done[w] & 1);
+                    if (!mbar_try_wait(bar_full + 8 * w, ph) || !mbar_try_wait(bar_tempty + 8 * w, ph ^ 1))
+                        continue;
+                    tc_fence_after();
+                    const uint32_t st = sbase + kOffK + w * kStageBytes;
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
-                            const uint32_t b_addr = a_addr + bt * kBoxBytes;
-                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(b_addr), kIdesc,
-                                       (kh | ks) ? 1u : 0u);
+                    for (int bt = 0; bt < 2; ++bt) {
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
+#pragma unroll
+                        for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks) {
+                                const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
+                                const uint32_t b_addr = a_addr + bt * kBoxBytes;
+                                tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(b_addr), kIdesc,
+                                           (kh | ks) ? 1u : 0u);
+                            }
                         }
                     }
+                    tc_commit(bar_empty + 8 * w);
+                    tc_commit(bar_tfull + 8 * w);
+                    ++done[w];
+                    progress = true;
                 }
-                tc_commit(bar_empty + 8 * s);
-                tc_commit(bar_tfull + 8 * w);
+                if (!pending) break;
+                if (progress) {
+                    t_last = global_timer();
+                } else if (global_timer() - t_last > kWaitNs) {
+                    record_timeout(p, abort_flag);
+                    break;
+                } else {
+                    __nanosleep(20);
+                }
             }
-            // The last pair's MMAs must be complete before TMEM is released.
-            if (q > 0) {
-                const int64_t r = q - 1;
-                const int w = static_cast<int>(r % kNumWG);
-                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
+            // Every warpgroup's last MMAs must be complete before TMEM is released.
+#pragma unroll
+            for (int w = 0; w < kNumWG; ++w) {
+                if (done[w] == 0) continue;
+                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((done[w] - 1) & 1)))
                     record_timeout(p, abort_flag);
             }
         }
