@@ -357,42 +357,23 @@ __device__ __forceinline__ void frag_from_acc(const float (&acc)[2][4], Frag16 &
 // step ks, n8 tile nt and this lane (g = lane / 4, t = lane % 4) the pair
 // (Bm[8ks + 2t][8nt + g], Bm[8ks + 2t + 1][8nt + g]) is the float2 at
 // rowp + (8 nt + g) * kAPitch + 8 ks + 2 t, i.e. Bm is the transpose of the
-// row-major 16x16 block at rowp.  The twelve mma.sync go to four accumulators
-// (k8 step x n8 tile) in term-major order, so dependent instructions are four
-// apart (longer than the mma.sync latency); the small cross terms come first.
+// row-major 16x16 block at rowp.
 __device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag16 &f,
                                                   const float *rowp, int g, int t) {
-    uint32_t bb[2][2][2], bs[2][2][2];   // [ks][nt][pair element]
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks)
+    for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const float2 b = *reinterpret_cast<const float2 *>(rowp + (8 * nt + g) * kAPitch +
                                                                8 * ks + 2 * t);
-            split_tf32(b.x, bb[ks][nt][0], bs[ks][nt][0]);
-            split_tf32(b.y, bb[ks][nt][1], bs[ks][nt][1]);
+            uint32_t bb0, bs0, bb1, bs1;
+            split_tf32(b.x, bb0, bs0);
+            split_tf32(b.y, bb1, bs1);
+            mma_tf32(acc[nt], f.small[ks], bb0, bb1);
+            mma_tf32(acc[nt], f.big[ks], bs0, bs1);
+            mma_tf32(acc[nt], f.big[ks], bb0, bb1);
         }
-    float part[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) part[nt][e] = 0.0f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[nt], f.small[0], bb[0][nt][0], bb[0][nt][1]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) mma_tf32(part[nt], f.small[1], bb[1][nt][0], bb[1][nt][1]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[nt], f.big[0], bs[0][nt][0], bs[0][nt][1]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) mma_tf32(part[nt], f.big[1], bs[1][nt][0], bs[1][nt][1]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) mma_tf32(acc[nt], f.big[0], bb[0][nt][0], bb[0][nt][1]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) mma_tf32(part[nt], f.big[1], bb[1][nt][0], bb[1][nt][1]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] += part[nt][e];
+    }
 }
 
 // Left operand D_JJ^T (= Z_JJ) read from its parking block.
@@ -459,36 +440,26 @@ __device__ __forceinline__ Tile pick(const Tile &a, const Tile &b, bool second) 
     return t;
 }
 
-// Per-row gate inputs of a tile, loaded one pair ahead and kept raw (no
-// arithmetic on them until they are used, so the loads stay in flight): this
-// row's g and beta, and the chunk's first and last g.
+// Per-row gate inputs of a tile, loaded one pair ahead: this row's g and beta
+// and the chunk's reference log-gate gref = (g_first + g_last) / 2.
 struct RowIn {
-    float g, gfirst, glast;
-    unsigned short beta;   // bf16 bits
+    float g, beta, gref;
 };
 
 __device__ __forceinline__ RowIn load_row(const Params &p, const Tile &t, int i) {
     RowIn r;
     r.g = 0.0f;
-    r.gfirst = 0.0f;
-    r.glast = 0.0f;
-    r.beta = 0;
+    r.beta = 0.0f;
+    r.gref = 0.0f;
     if (i < t.L) {
         const int64_t base = t.row0 * p.H + t.h;
         if (p.g) {
             r.g = __ldg(p.g + base + static_cast<int64_t>(i) * p.H);
-            r.gfirst = __ldg(p.g + base);
-            r.glast = __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H);
+            r.gref = 0.5f * (__ldg(p.g + base) + __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H));
         }
-        r.beta = p.beta ? __ldg(reinterpret_cast<const unsigned short *>(p.beta) + base +
-                                static_cast<int64_t>(i) * p.H)
-                        : static_cast<unsigned short>(0x3F80);   // bf16 1.0
+        r.beta = p.beta ? __bfloat162float(p.beta[base + static_cast<int64_t>(i) * p.H]) : 1.0f;
     }
     return r;
-}
-
-__device__ __forceinline__ float bf16_bits_to_float(unsigned short b) {
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
 __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
@@ -547,121 +518,84 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
                                 : 0;
 
-    // Warpgroup w owns pipeline stage w and TMEM columns [128 w, 128 w + 128) and
-    // processes the CTA-local pairs q = w, w + kNumWG, ...  The producer and the
-    // MMA issuer serve the warpgroups round-robin with non-blocking polls, so a
-    // slow warpgroup never holds up the others; each gives up after kWaitNs
-    // without progress.
-    static_assert(kNumStages == kNumWG, "one stage per warpgroup");
     if (warp == kProducerWarp) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
                          : "memory");
-            int64_t done[kNumWG];
-#pragma unroll
-            for (int w = 0; w < kNumWG; ++w) done[w] = 0;
-            uint64_t t_last = global_timer();
-            while (!*abort_flag) {
-                bool pending = false, progress = false;
-#pragma unroll
-                for (int w = 0; w < kNumWG; ++w) {
-                    const int64_t q = w + kNumWG * done[w];
-                    if (q >= n_local) continue;
-                    pending = true;
-                    const uint32_t ph = static_cast<uint32_t>(done[w] & 1);
-                    if (!mbar_try_wait(bar_empty + 8 * w, ph ^ 1)) continue;
-                    const int64_t pair = blockIdx.x + q * gridDim.x;
-                    const Tile t0 = tile_of(p, 2 * pair);
-                    const Tile t1 = tile_of(p, 2 * pair + 1);
-                    const uint32_t bytes = (t0.L > 0 ? 2 * kBoxBytes : 0) + (t1.L > 0 ? 2 * kBoxBytes : 0);
-                    const uint32_t st = sbase + kOffK + w * kStageBytes;
-                    mbar_arrive_expect_tx(bar_full + 8 * w, bytes);
-                    if (t0.L > 0) {
-                        tma_load_3d(st + 0 * kBoxBytes, &tmap_k, bar_full + 8 * w, 0, t0.h,
-                                    static_cast<int>(t0.row0));
-                        tma_load_3d(st + 2 * kBoxBytes, &tmap_k, bar_full + 8 * w, 64, t0.h,
-                                    static_cast<int>(t0.row0));
-                    }
-                    if (t1.L > 0) {
-                        tma_load_3d(st + 1 * kBoxBytes, &tmap_k, bar_full + 8 * w, 0, t1.h,
-                                    static_cast<int>(t1.row0));
-                        tma_load_3d(st + 3 * kBoxBytes, &tmap_k, bar_full + 8 * w, 64, t1.h,
-                                    static_cast<int>(t1.row0));
-                    }
-                    ++done[w];
-                    progress = true;
-                }
-                if (!pending) break;
-                if (progress) {
-                    t_last = global_timer();
-                } else if (global_timer() - t_last > kWaitNs) {
+            int64_t q = 0;
+            for (; q < n_local; ++q) {
+                if (*abort_flag) break;
+                const int s = static_cast<int>(q % kNumStages);
+                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
+                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
                     record_timeout(p, abort_flag);
                     break;
-                } else {
-                    __nanosleep(20);
+                }
+                const int64_t pair = blockIdx.x + q * gridDim.x;
+                const Tile t0 = tile_of(p, 2 * pair);
+                const Tile t1 = tile_of(p, 2 * pair + 1);
+                const uint32_t bytes = (t0.L > 0 ? 2 * kBoxBytes : 0) + (t1.L > 0 ? 2 * kBoxBytes : 0);
+                const uint32_t st = sbase + kOffK + s * kStageBytes;
+                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+                if (t0.L > 0) {
+                    tma_load_3d(st + 0 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t0.h,
+                                static_cast<int>(t0.row0));
+                    tma_load_3d(st + 2 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t0.h,
+                                static_cast<int>(t0.row0));
+                }
+                if (t1.L > 0) {
+                    tma_load_3d(st + 1 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t1.h,
+                                static_cast<int>(t1.row0));
+                    tma_load_3d(st + 3 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t1.h,
+                                static_cast<int>(t1.row0));
                 }
             }
             // Drain: every issued load has landed and every stage's MMAs committed.
-#pragma unroll
-            for (int w = 0; w < kNumWG; ++w) {
-                if (done[w] == 0) continue;
-                const uint32_t ph = static_cast<uint32_t>((done[w] - 1) & 1);
-                if (!mbar_wait(bar_full + 8 * w, ph)) record_timeout(p, abort_flag);
-                if (!mbar_wait(bar_empty + 8 * w, ph)) record_timeout(p, abort_flag);
+            const int64_t first = q > kNumStages ? q - kNumStages : 0;
+            for (int64_t r = first; r < q; ++r) {
+                const int s = static_cast<int>(r % kNumStages);
+                const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
+                if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
+                if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
             }
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            int64_t done[kNumWG];
-#pragma unroll
-            for (int w = 0; w < kNumWG; ++w) done[w] = 0;
-            uint64_t t_last = global_timer();
-            while (!*abort_flag) {
-                bool pending = false, progress = false;
-#pragma unroll
-                for (int w = 0; w < kNumWG; ++w) {
-                    const int64_t q = w + kNumWG * done[w];
-                    if (q >= n_local) continue;
-                    pending = true;
-                    const uint32_t ph = static_cast<uint32_t>(done[w] & 1);
-                    if (!mbar_try_wait(bar_full + 8 * w, ph) || !mbar_try_wait(bar_tempty + 8 * w, ph ^ 1))
-                        continue;
-                    tc_fence_after();
-                    const uint32_t st = sbase + kOffK + w * kStageBytes;
-#pragma unroll
-                    for (int bt = 0; bt < 2; ++bt) {
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
-#pragma unroll
-                        for (int kh = 0; kh < 2; ++kh) {
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks) {
-                                const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
-                                const uint32_t b_addr = a_addr + bt * kBoxBytes;
-                                tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(b_addr), kIdesc,
-                                           (kh | ks) ? 1u : 0u);
-                            }
-                        }
-                    }
-                    tc_commit(bar_empty + 8 * w);
-                    tc_commit(bar_tfull + 8 * w);
-                    ++done[w];
-                    progress = true;
-                }
-                if (!pending) break;
-                if (progress) {
-                    t_last = global_timer();
-                } else if (global_timer() - t_last > kWaitNs) {
+            int64_t q = 0;
+            for (; q < n_local; ++q) {
+                if (*abort_flag) break;
+                const int s = static_cast<int>(q % kNumStages);
+                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
+                const int w = static_cast<int>(q % kNumWG);
+                const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
+                if (!mbar_wait(bar_full + 8 * s, ph) || !mbar_wait(bar_tempty + 8 * w, phw ^ 1)) {
                     record_timeout(p, abort_flag);
                     break;
-                } else {
-                    __nanosleep(20);
                 }
-            }
-            // Every warpgroup's last MMAs must be complete before TMEM is released.
+                tc_fence_after();
+                const uint32_t st = sbase + kOffK + s * kStageBytes;
 #pragma unroll
-            for (int w = 0; w < kNumWG; ++w) {
-                if (done[w] == 0) continue;
-                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((done[w] - 1) & 1)))
+                for (int bt = 0; bt < 2; ++bt) {
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
+#pragma unroll
+                    for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
+                            const uint32_t b_addr = a_addr + bt * kBoxBytes;
+                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(b_addr), kIdesc,
+                                       (kh | ks) ? 1u : 0u);
+                        }
+                    }
+                }
+                tc_commit(bar_empty + 8 * s);
+                tc_commit(bar_tfull + 8 * w);
+            }
+            // The last pair's MMAs must be complete before TMEM is released.
+            if (q > 0) {
+                const int64_t r = q - 1;
+                const int w = static_cast<int>(r % kNumWG);
+                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
                     record_timeout(p, abort_flag);
             }
         }
@@ -714,7 +648,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             float ui = 1.0f, vi = 1.0f;
             bool unsafe = false;
             if (p.g && rowok) {
-                const float d = rin.g - 0.5f * (rin.gfirst + rin.glast);
+                const float d = rin.g - rin.gref;
                 unsafe = !(fabsf(d) <= 30.0f);
                 ui = expf(d);
                 vi = expf(-d);
@@ -753,7 +687,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = z;
                 } else if (!direct) {
-                    const float w = bf16_bits_to_float(rin.beta) * ui;
+                    const float w = rin.beta * ui;
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
@@ -767,7 +701,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                     }
                 } else {
-                    const float gi = rin.g, bi = bf16_bits_to_float(rin.beta);
+                    const float gi = rin.g, bi = rin.beta;
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
