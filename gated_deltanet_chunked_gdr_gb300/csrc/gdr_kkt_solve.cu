@@ -58,7 +58,8 @@ constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][1
 constexpr int kAPitch = 68;                         // floats per A row (68*4 = 272 B)
 constexpr int kATileBytes = kChunk * kAPitch * 4;   // 17408
 constexpr int kATile1Off = kATileBytes + 16;        // second tile shifted by 16 B (other banks)
-constexpr int kAWGBytes = 34944;                    // >= kATile1Off + kATileBytes, multiple of 128
+constexpr int kAWGBytes = 35840;                    // >= kATile1Off + kATileBytes, multiple of 1024
+constexpr int kStage1Off = 17408;                   // output staging of the second tile (1024-aligned)
 constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
 constexpr uint32_t kTmemCols = 512;
 
@@ -328,9 +329,13 @@ struct Frag16 {
     uint32_t small[2][4];
 };
 
+// x = big + small exactly: big is x rounded to tf32 (ten mantissa bits, round
+// half away from zero, done on the bit pattern: add half an ulp of tf32, clear
+// the 13 low bits), small = x - big with |small| <= 2^-11 |x|; the tensor core
+// reads small to tf32 precision, so the split products carry ~2^-21 relative
+// error.  Integer arithmetic keeps the split on the full-rate ALU pipes.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &big, uint32_t &small) {
-    uint32_t b;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(x));
+    const uint32_t b = (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
     big = b;
     small = __float_as_uint(x - __uint_as_float(b));
 }
@@ -414,6 +419,87 @@ __device__ __forceinline__ void merge_column(const float *At, int g, int t,
     }
 }
 
+// ------------------------------------------------------------ output staging
+// X is assembled in the layout a 128-byte-swizzled TMA store reads: a tile's 64
+// rows of 128 bytes (bf16: 64 values; fp32: two 32-value halves 8 KB apart), the
+// 16-byte piece q of row r stored at piece position q ^ (r % 8).
+template <bool BF16>
+__device__ __forceinline__ uint32_t stage_piece_off(int r, int q) {
+    if (BF16) return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
+    return static_cast<uint32_t>((q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4));
+}
+
+template <bool BF16>
+__device__ __forceinline__ void stage_put(uint8_t *st, int r, int c, float v) {
+    if (BF16) {
+        *reinterpret_cast<__nv_bfloat16 *>(st + stage_piece_off<true>(r, c >> 3) + 2 * (c & 7)) =
+            __float2bfloat16_rn(v);
+    } else {
+        *reinterpret_cast<float *>(st + stage_piece_off<false>(r, c >> 2) + 4 * (c & 3)) = v;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Row r of X restricted to columns >= 16 I: the diagonal block row (d[0..3] =
+// 16 values) followed by zeros.
+template <bool BF16>
+__device__ __forceinline__ void stage_diag_row(uint8_t *st, int r, int I, const float4 (&d)[4]) {
+    if (BF16) {
+        uint4 a, b;
+        a.x = pack_bf16x2(d[0].x, d[0].y); a.y = pack_bf16x2(d[0].z, d[0].w);
+        a.z = pack_bf16x2(d[1].x, d[1].y); a.w = pack_bf16x2(d[1].z, d[1].w);
+        b.x = pack_bf16x2(d[2].x, d[2].y); b.y = pack_bf16x2(d[2].z, d[2].w);
+        b.z = pack_bf16x2(d[3].x, d[3].y); b.w = pack_bf16x2(d[3].z, d[3].w);
+        *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I)) = a;
+        *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I + 1)) = b;
+#pragma unroll
+        for (int q = 2; q < 8; ++q)
+            if (q >= 2 * I + 2) *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, q)) = make_uint4(0, 0, 0, 0);
+    } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4 *>(st + stage_piece_off<false>(r, 4 * I + m)) = d[m];
+#pragma unroll
+        for (int q = 4; q < 16; ++q)
+            if (q >= 4 * I + 4)
+                *reinterpret_cast<float4 *>(st + stage_piece_off<false>(r, q)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Z_JI (accumulator layout) -> rows 16I.. / columns 16J.. of X in the staging.
+template <bool BF16>
+__device__ __forceinline__ void stage_block_T(uint8_t *st, int I, int J, const float (&z)[2][4],
+                                              int g, int t) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int r0 = 16 * I + 8 * nt + 2 * t, c0 = 16 * J + g;
+        stage_put<BF16>(st, r0, c0, z[nt][0]);
+        stage_put<BF16>(st, r0 + 1, c0, z[nt][1]);
+        stage_put<BF16>(st, r0, c0 + 8, z[nt][2]);
+        stage_put<BF16>(st, r0 + 1, c0 + 8, z[nt][3]);
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Writes Z_JI (accumulator layout) into rows 16I.. / columns 16J.. of X.
 __device__ __forceinline__ void store_block_T(float *At, int I, int J, const float (&z)[2][4],
                                               int g, int t) {
@@ -477,7 +563,8 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
 
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(kNumThreads, 1)
-    kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k, const Params p) {
+    kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_out, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -634,6 +721,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const RowIn rnext = load_row(p, pick(nx0, nx1, tt_e), i_e);
 
             if (qd == 0 && lane == 0) {
+                bulk_wait_read();
                 int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
                 wg_flag[wg] = ok;
@@ -738,72 +826,64 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column);
             //      then X rows are assembled in the A buffer (after B4 in both branches)
             const int mt = qd & 1;
+            uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
             if (qd < 2) {
                 float z0[3][2][4];
                 merge_column<0>(At(mt), g8, t4, z0);
                 named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                store_block_T(At(mt), 1, 0, z0[0], g8, t4);
-                store_block_T(At(mt), 2, 0, z0[1], g8, t4);
-                store_block_T(At(mt), 3, 0, z0[2], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, 1, 0, z0[0], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, 2, 0, z0[1], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, 3, 0, z0[2], g8, t4);
             } else {
                 float z1[2][2][4], z2[1][2][4];
                 merge_column<1>(At(mt), g8, t4, z1);
                 merge_column<2>(At(mt), g8, t4, z2);
                 named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                store_block_T(At(mt), 2, 1, z1[0], g8, t4);
-                store_block_T(At(mt), 3, 1, z1[1], g8, t4);
-                store_block_T(At(mt), 3, 2, z2[0], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, 2, 1, z1[0], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, 3, 1, z1[1], g8, t4);
+                stage_block_T<OUT_BF16>(st_m, 3, 2, z2[0], g8, t4);
             }
             {
-                float4 *row = reinterpret_cast<float4 *>(At(dt) + (16 * dI + dc) * kAPitch);
-                row[4 * dI + 0] = make_float4(drow[0], drow[1], drow[2], drow[3]);
-                row[4 * dI + 1] = make_float4(drow[4], drow[5], drow[6], drow[7]);
-                row[4 * dI + 2] = make_float4(drow[8], drow[9], drow[10], drow[11]);
-                row[4 * dI + 3] = make_float4(drow[12], drow[13], drow[14], drow[15]);
-                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int j4 = 4; j4 < 16; ++j4)
-                    if (j4 >= 4 * dI + 4) row[j4] = z;
+                const float4 dv[4] = {make_float4(drow[0], drow[1], drow[2], drow[3]),
+                                      make_float4(drow[4], drow[5], drow[6], drow[7]),
+                                      make_float4(drow[8], drow[9], drow[10], drow[11]),
+                                      make_float4(drow[12], drow[13], drow[14], drow[15])};
+                stage_diag_row<OUT_BF16>(abuf + (dt ? kStage1Off : 0), 16 * dI + dc, dI, dv);
             }
+            fence_proxy_async_smem();
             named_bar_sync(bar_id, 128);                       // B5: X complete
 
-            // ---- coalesced 16-byte stores: warp -> 32 rows of one tile
+            // ---- store: full chunks by TMA from the staging, partial chunks row by row
+            if (tid == 0) {
+                bool any = false;
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2) {
+                    const Tile ts = pick(cur0, cur1, t2);
+                    if (ts.L == kChunk) {
+                        const uint32_t src = smem_u32(abuf + (t2 ? kStage1Off : 0));
+                        tma_store_3d(&tmap_out, src, 0, ts.h, static_cast<int>(ts.row0));
+                        if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, ts.h, static_cast<int>(ts.row0));
+                        any = true;
+                    }
+                }
+                if (any) bulk_commit();
+            }
             {
                 const int st_t = qd >> 1;
                 const Tile ts = pick(cur0, cur1, st_t);
-                const float *Xs = At(st_t);
-                if (OUT_BF16) {
-#pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = 32 * (qd & 1) + 4 * it + (lane >> 3);
-                        const int piece = lane & 7;
-                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece);
-                        const float4 b = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 8 * piece + 4);
+                if (ts.L > 0 && ts.L < kChunk) {
+                    const uint8_t *sb = abuf + (st_t ? kStage1Off : 0);
+                    constexpr int kPieces = OUT_BF16 ? 8 : 16;
+                    constexpr int kRowsPerIt = 32 / kPieces;
+#pragma unroll 2
+                    for (int it = 0; it < 32 / kRowsPerIt; ++it) {
+                        const int rr = 32 * (qd & 1) + kRowsPerIt * it + lane / kPieces;
+                        const int piece = lane % kPieces;
                         if (rr < ts.L) {
-                            __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y);
-                            __nv_bfloat162 h1 = __floats2bfloat162_rn(a.z, a.w);
-                            __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y);
-                            __nv_bfloat162 h3 = __floats2bfloat162_rn(b.z, b.w);
-                            uint4 v;
-                            v.x = *reinterpret_cast<uint32_t *>(&h0);
-                            v.y = *reinterpret_cast<uint32_t *>(&h1);
-                            v.z = *reinterpret_cast<uint32_t *>(&h2);
-                            v.w = *reinterpret_cast<uint32_t *>(&h3);
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sb + stage_piece_off<OUT_BF16>(rr, piece));
                             const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
-                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 128 +
-                                                       16 * piece) = v;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int it = 0; it < 16; ++it) {
-                        const int rr = 32 * (qd & 1) + 2 * it + (lane >> 4);
-                        const int piece = lane & 15;
-                        const float4 a = *reinterpret_cast<const float4 *>(Xs + rr * kAPitch + 4 * piece);
-                        if (rr < ts.L) {
-                            const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
-                            *reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(p.out) + orow * 256 +
-                                                        16 * piece) = a;
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
+                                                       orow * (OUT_BF16 ? 128 : 256) + 16 * piece) = v;
                         }
                     }
                 }
@@ -812,6 +892,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             cur1 = nx1;
             rin = rnext;
         }
+        if (tid == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -932,6 +1013,19 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GDR_ERR_CUDA;
 
+    CUtensorMap tmap_o;
+    {
+        const int esz = out_dtype == GDR_BF16 ? 2 : 4;
+        const cuuint64_t odims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(ntok)};
+        const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(64 * esz), static_cast<cuuint64_t>(H * 64 * esz)};
+        const cuuint32_t obox[3] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(kChunk)};
+        if (encode(&tmap_o, out_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GDR_ERR_CUDA;
+    }
+
     Params prm;
     prm.g = g;
     prm.beta = static_cast<const __nv_bfloat16 *>(beta);
@@ -956,9 +1050,9 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
     const int64_t grid = prm.n_pairs < sms ? prm.n_pairs : sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (out_dtype == GDR_BF16)
-        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
+        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     else
-        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, prm);
+        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }
