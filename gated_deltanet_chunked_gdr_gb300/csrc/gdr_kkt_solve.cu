@@ -285,9 +285,11 @@ __device__ __forceinline__ Tile tile_of(const Params &p, int64_t u) {
 //   D_II = (I + A_II)^{-1}                       for the four diagonal blocks,
 //   X_IJ = -D_II * sum_{M=J}^{I-1} A_IM X_MJ     for the six blocks below them.
 // The diagonal blocks use fp32 forward substitution on CUDA cores (one lane per
-// row).  The off-diagonal products run on tensor cores as 3xTF32 mma.sync
-// (x = big + small, both tf32; big*big + big*small + small*big), which keeps
-// them fp32-accurate.  They are evaluated transposed, Z_JI = X_IJ^T =
+// row).  The off-diagonal products run on tensor cores with mma.sync tf32: for
+// fp32 output as 3xTF32 (x = big + small, both tf32; big*big + big*small +
+// small*big), which keeps them fp32-accurate; for bf16 output as one tf32
+// pass, whose error (max ~2e-4 on the workloads, fp64 emulation) is below the
+// bf16 rounding of the result.  They are evaluated transposed, Z_JI = X_IJ^T =
 // -(sum_M Z_JM A_IM^T) D_II^T, so every product's left operand is the previous
 // product's accumulator.
 
@@ -349,12 +351,18 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// SPLIT = false keeps the raw fp32 bits in f.big (the tensor core reads them as
+// tf32) for a single-pass product; f.small is unused then.
+template <bool SPLIT>
 __device__ __forceinline__ void frag_from_acc(const float (&acc)[2][4], Frag16 &f) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         const float v[4] = {acc[ks][0], acc[ks][2], acc[ks][1], acc[ks][3]};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_tf32(v[e], f.big[ks][e], f.small[ks][e]);
+        for (int e = 0; e < 4; ++e) {
+            if (SPLIT) split_tf32(v[e], f.big[ks][e], f.small[ks][e]);
+            else f.big[ks][e] = __float_as_uint(v[e]);
+        }
     }
 }
 
@@ -363,6 +371,7 @@ __device__ __forceinline__ void frag_from_acc(const float (&acc)[2][4], Frag16 &
 // (Bm[8ks + 2t][8nt + g], Bm[8ks + 2t + 1][8nt + g]) is the float2 at
 // rowp + (8 nt + g) * kAPitch + 8 ks + 2 t, i.e. Bm is the transpose of the
 // row-major 16x16 block at rowp.
+template <bool SPLIT>
 __device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag16 &f,
                                                   const float *rowp, int g, int t) {
 #pragma unroll
@@ -371,17 +380,22 @@ __device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag
         for (int nt = 0; nt < 2; ++nt) {
             const float2 b = *reinterpret_cast<const float2 *>(rowp + (8 * nt + g) * kAPitch +
                                                                8 * ks + 2 * t);
-            uint32_t bb0, bs0, bb1, bs1;
-            split_tf32(b.x, bb0, bs0);
-            split_tf32(b.y, bb1, bs1);
-            mma_tf32(acc[nt], f.small[ks], bb0, bb1);
-            mma_tf32(acc[nt], f.big[ks], bs0, bs1);
-            mma_tf32(acc[nt], f.big[ks], bb0, bb1);
+            if (SPLIT) {
+                uint32_t bb0, bs0, bb1, bs1;
+                split_tf32(b.x, bb0, bs0);
+                split_tf32(b.y, bb1, bs1);
+                mma_tf32(acc[nt], f.small[ks], bb0, bb1);
+                mma_tf32(acc[nt], f.big[ks], bs0, bs1);
+                mma_tf32(acc[nt], f.big[ks], bb0, bb1);
+            } else {
+                mma_tf32(acc[nt], f.big[ks], __float_as_uint(b.x), __float_as_uint(b.y));
+            }
         }
     }
 }
 
 // Left operand D_JJ^T (= Z_JJ) read from its parking block.
+template <bool SPLIT>
 __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag16 &f) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
@@ -389,13 +403,16 @@ __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag1
                             D[(8 * ks + 2 * t + 1) * kAPitch + g],
                             D[(8 * ks + 2 * t + 1) * kAPitch + g + 8]};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_tf32(v[e], f.big[ks][e], f.small[ks][e]);
+        for (int e = 0; e < 4; ++e) {
+            if (SPLIT) split_tf32(v[e], f.big[ks][e], f.small[ks][e]);
+            else f.big[ks][e] = __float_as_uint(v[e]);
+        }
     }
 }
 
 // Blocks Z_JI = X_IJ^T for I = J+1..3 of one tile (At = its A buffer).  Split
 // operands are rebuilt when needed instead of cached, to stay within registers.
-template <int J>
+template <int J, bool SPLIT>
 __device__ __forceinline__ void merge_column(const float *At, int g, int t,
                                              float (&Z)[3 - J][2][4]) {
 #pragma unroll
@@ -404,14 +421,14 @@ __device__ __forceinline__ void merge_column(const float *At, int g, int t,
 #pragma unroll
         for (int M = J; M < I; ++M) {
             Frag16 f;
-            if (M == J) frag_from_dT(At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J), g, t, f);
-            else frag_from_acc(Z[M - J - 1], f);
-            mma3_times_blockT(acc, f, At + 16 * I * kAPitch + 16 * M, g, t);
+            if (M == J) frag_from_dT<SPLIT>(At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J), g, t, f);
+            else frag_from_acc<SPLIT>(Z[M - J - 1], f);
+            mma3_times_blockT<SPLIT>(acc, f, At + 16 * I * kAPitch + 16 * M, g, t);
         }
         Frag16 rf;
-        frag_from_acc(acc, rf);
+        frag_from_acc<SPLIT>(acc, rf);
         float z[2][4] = {};
-        mma3_times_blockT(z, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
+        mma3_times_blockT<SPLIT>(z, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -829,15 +846,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
             if (qd < 2) {
                 float z0[3][2][4];
-                merge_column<0>(At(mt), g8, t4, z0);
+                merge_column<0, !OUT_BF16>(At(mt), g8, t4, z0);
                 named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
                 stage_block_T<OUT_BF16>(st_m, 1, 0, z0[0], g8, t4);
                 stage_block_T<OUT_BF16>(st_m, 2, 0, z0[1], g8, t4);
                 stage_block_T<OUT_BF16>(st_m, 3, 0, z0[2], g8, t4);
             } else {
                 float z1[2][2][4], z2[1][2][4];
-                merge_column<1>(At(mt), g8, t4, z1);
-                merge_column<2>(At(mt), g8, t4, z2);
+                merge_column<1, !OUT_BF16>(At(mt), g8, t4, z1);
+                merge_column<2, !OUT_BF16>(At(mt), g8, t4, z2);
                 named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
                 stage_block_T<OUT_BF16>(st_m, 2, 1, z1[0], g8, t4);
                 stage_block_T<OUT_BF16>(st_m, 3, 1, z1[1], g8, t4);
