@@ -543,26 +543,36 @@ __device__ __forceinline__ Tile pick(const Tile &a, const Tile &b, bool second) 
     return t;
 }
 
-// Per-row gate inputs of a tile, loaded one pair ahead: this row's g and beta
-// and the chunk's reference log-gate gref = (g_first + g_last) / 2.
+// Per-row gate inputs of a tile, loaded one pair ahead and kept raw (no
+// arithmetic on them until they are used, so the loads stay in flight): this
+// row's g and beta, and the chunk's first and last g.
 struct RowIn {
-    float g, beta, gref;
+    float g, gfirst, glast;
+    unsigned short beta;   // bf16 bits
 };
 
 __device__ __forceinline__ RowIn load_row(const Params &p, const Tile &t, int i) {
     RowIn r;
     r.g = 0.0f;
-    r.beta = 0.0f;
-    r.gref = 0.0f;
+    r.gfirst = 0.0f;
+    r.glast = 0.0f;
+    r.beta = 0;
     if (i < t.L) {
         const int64_t base = t.row0 * p.H + t.h;
         if (p.g) {
             r.g = __ldg(p.g + base + static_cast<int64_t>(i) * p.H);
-            r.gref = 0.5f * (__ldg(p.g + base) + __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H));
+            r.gfirst = __ldg(p.g + base);
+            r.glast = __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H);
         }
-        r.beta = p.beta ? __bfloat162float(p.beta[base + static_cast<int64_t>(i) * p.H]) : 1.0f;
+        r.beta = p.beta ? __ldg(reinterpret_cast<const unsigned short *>(p.beta) + base +
+                                static_cast<int64_t>(i) * p.H)
+                        : static_cast<unsigned short>(0x3F80);   // bf16 1.0
     }
     return r;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(unsigned short b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
 __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
@@ -753,7 +763,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             float ui = 1.0f, vi = 1.0f;
             bool unsafe = false;
             if (p.g && rowok) {
-                const float d = rin.g - rin.gref;
+                const float d = rin.g - 0.5f * (rin.gfirst + rin.glast);
                 unsafe = !(fabsf(d) <= 30.0f);
                 ui = expf(d);
                 vi = expf(-d);
@@ -792,7 +802,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = z;
                 } else if (!direct) {
-                    const float w = rin.beta * ui;
+                    const float w = bf16_bits_to_float(rin.beta) * ui;
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
@@ -806,7 +816,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                     }
                 } else {
-                    const float gi = rin.g, bi = rin.beta;
+                    const float gi = rin.g, bi = bf16_bits_to_float(rin.beta);
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
