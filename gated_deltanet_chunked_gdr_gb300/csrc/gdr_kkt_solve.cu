@@ -800,7 +800,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (!rowok) {
                     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int j4 = 0; j4 < 16; ++j4) Arow[j4] = z;
+                    for (int j4 = 0; j4 < 16; ++j4)
+                        if (j4 < n4) Arow[j4] = z;
                 } else if (!direct) {
                     const float w = bf16_bits_to_float(rin.beta) * ui;
 #pragma unroll
@@ -835,7 +836,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            named_bar_sync(bar_id, 128);                       // B3: A complete
+            // The diagonal blocks this warp inverts below are exactly the 32 rows it
+            // has just written (tile qd >> 1, rows 32 (qd & 1) ..), so a warp-level
+            // barrier is enough here.
+            __syncwarp();
 
             // ---- diagonal inverses: thread -> (tile, block I, row c)
             const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
