@@ -8,26 +8,29 @@
 // (I+A)^{-1} of shape [B, T, H, 64]).  The intermediate A never leaves the SM
 // and no separate zero-fill pass runs.
 //
-// Kernel organisation (one persistent CTA per SM, 14 warps):
-//   warp 12      producer: walks the tile schedule and TMA-loads the key tiles of
-//                two (chunk, head) tiles per pipeline stage (bf16, 128-byte swizzle).
+// Kernel organisation (one persistent CTA per SM, 14 warps; a CTA takes the tile
+// pairs blockIdx.x, blockIdx.x + grid, ...):
+//   warp 12      producer: lanes 0-1 TMA-load the key tiles of the next pair's two
+//                (chunk, head) tiles into a three-stage ring (bf16, 128-byte
+//                swizzle, 32 KB per stage); lanes 2-3 prefetch into L2 the keys of
+//                the pair two steps further on.
 //   warp 13      MMA issuer: allocates TMEM and, per stage, issues tcgen05.mma
-//                (kind::f16, M=128 = both tiles' 64 rows, N=64 = one tile's rows,
-//                K=128) twice, so TMEM holds K0*K0^T and K1*K1^T in fp32.
+//                (kind::f16, M = N = 128 = both tiles' rows, K = 128 in 8 steps),
+//                so TMEM holds the pair's 128 x 128 Gram matrix in fp32; each tile
+//                reads its own 64 x 64 diagonal block.
 //   warps 0..11  three consumer warpgroups; each owns 128 TMEM columns and one
 //                tile pair at a time:
 //                  epilogue - each thread reads its row of S = K*K^T from TMEM,
-//                             applies beta_i, exp(g_i - g_j) (exponent clamped to
-//                             [-50, 50] as in the page's bot summary) and writes
-//                             row i of A to shared memory;
-//                  solve    - each lane owns one output row c and runs a
-//                             right-looking substitution for row c of (I+A)^{-1}
-//                             in fp32 registers; warps take the 16-row blocks of
-//                             the chunk (the page's 16x16 sub-blocks BC=16) in a
-//                             rotating order so the triangular work spreads evenly;
-//                  store    - rows are staged in shared memory and written with
-//                             coalesced 128-bit stores (rows past the chunk end are
-//                             not written, zero columns are written explicitly).
+//                             applies beta_i and exp(g_i - g_j) (exponent clamped
+//                             to [-50, 50] as in the page's bot summary) and writes
+//                             row i of A to shared memory (fp32);
+//                  solve    - the page's 16 x 16 sub-blocks (BC = 16): the four
+//                             diagonal inverses by substitution on CUDA cores (one
+//                             lane per row), the six blocks below them on tensor
+//                             cores (mma.sync tf32);
+//                  store    - X is assembled in a 128-byte-swizzled staging copy
+//                             and written by TMA (full chunks) or by 128-bit
+//                             stores (a chunk cut short by the sequence end).
 // Every mbarrier wait is bounded by wall time; on expiry the kernel records
 // GDR_ERR_TIMEOUT in a device status word and all roles leave their loops.
 
@@ -62,6 +65,7 @@ constexpr int kAWGBytes = 35840;                    // >= kATile1Off + kATileByt
 constexpr int kStage1Off = 17408;                   // output staging of the second tile (1024-aligned)
 constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
 constexpr uint32_t kTmemCols = 512;
+constexpr int kPrefetchPairs = 2;         // L2 prefetch distance of the key tiles, in pairs
 
 constexpr int kOffK = 0;
 constexpr int kOffA = kOffK + kNumStages * kStageBytes;
@@ -76,6 +80,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffA % 1024 == 0, "stages must keep 1024-byte alignment");
 
 constexpr uint64_t kWaitNs = 2000000000ull;         // 2 s bound for every wait
+constexpr uint32_t kSuspendNs = 1000000;             // a waiting thread sleeps until the phase completes (or 1 ms)
 
 // Division by an invariant divisor d >= 1 for numerators n < 2^31 (Granlund and
 // Montgomery, "Division by invariant integers using multiplication", 1994): with
@@ -111,6 +116,8 @@ struct Params {
     int64_t n_pairs;   // ceil(n_slots * H / 2)
     FastDiv divH;      // tile -> (slot, head)
     FastDiv divNT;     // slot -> (sequence, chunk), fixed-length
+    uint32_t pair_ds, pair_dh;   // stride between a CTA's consecutive pairs (2 * grid tiles) as (slots, heads)
+    uint32_t wg_ds, wg_dh;       // stride between a warpgroup's consecutive pairs (2 * grid * warpgroups tiles)
     int *status;
 };
 
@@ -145,10 +152,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -168,6 +175,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -237,42 +250,101 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(2) << 61;
     return d;
 }
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N=64, M=128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) |
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N=128, M=128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
                             ((128u >> 4) << 24);
 
 // ------------------------------------------------------------ tile schedule
 // Tile u = slot * H + h.  Fixed-length: slot = b * NT + c.  Varlen: sequence n
 // owns the slots [base(n), base(n+1)) with base(n) = floor((cu[n] + 63 n) / 64),
 // which leaves room for its ceil(len/64) chunks (at most one slot stays empty).
-__device__ __forceinline__ Tile tile_of(const Params &p, int64_t u) {
+// The tiles a role visits form an arithmetic sequence u, u + S, u + 2S, ...
+// (S = 2 * grid tiles for the producer's pairs, 2 * grid * warpgroups for one
+// warpgroup's).  TileWalk keeps u's (slot, h) and the slot's (sequence, chunk)
+// and steps them by S = ds * H + dh with one carry: fixed-length moves the chunk
+// index and divides only when it passes NT; varlen moves the sequence index
+// forward over the boundaries base(n + 1) the slot has passed (base is
+// non-decreasing in n, so this finds the same sequence as a binary search).
+struct TileWalk {
+    uint32_t slot, h;
+    uint32_t b, c;          // fixed-length: slot = b * NT + c
+    int32_t n, s, e;        // varlen: sequence n of the slot, cu[n], cu[n + 1]
+    int64_t bn1;            // varlen: base(n + 1)
+};
+
+__device__ __forceinline__ TileWalk walk_init(const Params &p, uint32_t u) {
+    TileWalk w;
+    w.slot = p.divH.div(u);
+    w.h = u - w.slot * p.divH.d;
+    w.b = w.c = 0;
+    w.n = static_cast<int32_t>(p.B);
+    w.s = w.e = 0;
+    w.bn1 = 0;
+    if (p.cu == nullptr) {
+        w.b = p.divNT.div(w.slot);
+        w.c = w.slot - w.b * p.divNT.d;
+    } else if (w.slot < static_cast<uint64_t>(p.n_slots)) {
+        int64_t lo = 0, hi = p.B;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            const int64_t bm = (static_cast<int64_t>(__ldg(p.cu + mid)) + 63 * mid) >> 6;
+            if (bm <= w.slot) lo = mid;
+            else hi = mid - 1;
+        }
+        w.n = static_cast<int32_t>(lo);
+        if (lo < p.B) {
+            w.s = __ldg(p.cu + lo);
+            w.e = __ldg(p.cu + lo + 1);
+            w.bn1 = (static_cast<int64_t>(w.e) + 63 * (lo + 1)) >> 6;
+        }
+    }
+    return w;
+}
+
+__device__ __forceinline__ void walk_advance(const Params &p, TileWalk &w, uint32_t ds, uint32_t dh) {
+    uint32_t inc = ds;
+    w.h += dh;
+    if (w.h >= p.divH.d) {
+        w.h -= p.divH.d;
+        ++inc;
+    }
+    w.slot += inc;
+    if (p.cu == nullptr) {
+        w.c += inc;
+        if (w.c >= p.divNT.d) {
+            const uint32_t qd = p.divNT.div(w.c);
+            w.b += qd;
+            w.c -= qd * p.divNT.d;
+        }
+    } else {
+        // At most B steps over the whole walk; never reads past cu[B].
+        while (w.n < p.B && w.bn1 <= static_cast<int64_t>(w.slot)) {
+            ++w.n;
+            w.s = w.e;
+            if (w.n < p.B) {
+                w.e = __ldg(p.cu + w.n + 1);
+                w.bn1 = (static_cast<int64_t>(w.e) + 63 * static_cast<int64_t>(w.n + 1)) >> 6;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ Tile walk_tile(const Params &p, const TileWalk &w) {
     Tile t;
     t.row0 = 0;
     t.L = 0;
-    const uint32_t uu = static_cast<uint32_t>(u);          // u < 2^31 (checked on the host)
-    const uint32_t slot = p.divH.div(uu);
-    t.h = static_cast<int>(uu - slot * p.divH.d);
-    if (slot >= static_cast<uint64_t>(p.n_slots)) return t;
+    t.h = static_cast<int>(w.h);
+    if (w.slot >= static_cast<uint64_t>(p.n_slots)) return t;
     if (p.cu == nullptr) {
-        const uint32_t b = p.divNT.div(slot);
-        const uint32_t c = slot - b * p.divNT.d;
-        t.row0 = static_cast<int64_t>(b) * p.T + static_cast<int64_t>(c) * kChunk;
-        const int64_t rem = p.T - static_cast<int64_t>(c) * kChunk;
+        t.row0 = static_cast<int64_t>(w.b) * p.T + static_cast<int64_t>(w.c) * kChunk;
+        const int64_t rem = p.T - static_cast<int64_t>(w.c) * kChunk;
         t.L = static_cast<int>(rem < kChunk ? rem : kChunk);
         return t;
     }
-    int64_t lo = 0, hi = p.B;
-    while (lo < hi) {
-        const int64_t mid = (lo + hi + 1) >> 1;
-        const int64_t bm = (static_cast<int64_t>(__ldg(p.cu + mid)) + 63 * mid) >> 6;
-        if (bm <= slot) lo = mid;
-        else hi = mid - 1;
-    }
-    if (lo >= p.B) return t;
-    const int64_t s = __ldg(p.cu + lo);
-    int64_t e = __ldg(p.cu + lo + 1);
-    if (e > p.T) e = p.T;
-    const int64_t c = static_cast<int64_t>(slot) - ((s + 63 * lo) >> 6);
+    if (w.n >= p.B) return t;
+    const int64_t s = w.s;
+    const int64_t e = w.e > p.T ? p.T : w.e;
+    const int64_t c = static_cast<int64_t>(w.slot) - ((s + 63 * static_cast<int64_t>(w.n)) >> 6);
     const int64_t r0 = s + c * kChunk;
     if (c < 0 || s < 0 || r0 >= e) return t;
     t.row0 = r0;
@@ -488,16 +560,33 @@ __device__ __forceinline__ void stage_diag_row(uint8_t *st, int r, int I, const 
 }
 
 // Z_JI (accumulator layout) -> rows 16I.. / columns 16J.. of X in the staging.
+// bf16: one transposing matrix store; the accumulator pairs (z[nt][0], z[nt][1])
+// and (z[nt][2], z[nt][3]) are the fragments of four 8x8 matrices, stored
+// transposed, whose rows (X rows 16I + 8 (m / 2) + b, 16-byte piece 2J + m % 2)
+// are addressed by lane 8m + b.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
 template <bool BF16>
 __device__ __forceinline__ void stage_block_T(uint8_t *st, int I, int J, const float (&z)[2][4],
                                               int g, int t) {
+    if (BF16) {
+        const int lane = 4 * g + t, m = lane >> 3, b = lane & 7;
+        const uint32_t addr = smem_u32(st + stage_piece_off<true>(16 * I + 8 * (m >> 1) + b, 2 * J + (m & 1)));
+        stmatrix_x4_trans(addr, pack_bf16x2(z[0][0], z[0][1]), pack_bf16x2(z[0][2], z[0][3]),
+                          pack_bf16x2(z[1][0], z[1][1]), pack_bf16x2(z[1][2], z[1][3]));
+    } else {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int r0 = 16 * I + 8 * nt + 2 * t, c0 = 16 * J + g;
-        stage_put<BF16>(st, r0, c0, z[nt][0]);
-        stage_put<BF16>(st, r0 + 1, c0, z[nt][1]);
-        stage_put<BF16>(st, r0, c0 + 8, z[nt][2]);
-        stage_put<BF16>(st, r0 + 1, c0 + 8, z[nt][3]);
+        for (int nt = 0; nt < 2; ++nt) {
+            const int r0 = 16 * I + 8 * nt + 2 * t, c0 = 16 * J + g;
+            stage_put<false>(st, r0, c0, z[nt][0]);
+            stage_put<false>(st, r0 + 1, c0, z[nt][1]);
+            stage_put<false>(st, r0, c0 + 8, z[nt][2]);
+            stage_put<false>(st, r0 + 1, c0 + 8, z[nt][3]);
+        }
     }
 }
 
@@ -533,14 +622,6 @@ __device__ __forceinline__ void store_block_T(float *At, int I, int J, const flo
 __device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag) {
     *abort_flag = 1;
     atomicExch(p.status, static_cast<int>(GDR_ERR_TIMEOUT));
-}
-
-__device__ __forceinline__ Tile pick(const Tile &a, const Tile &b, bool second) {
-    Tile t;
-    t.row0 = second ? b.row0 : a.row0;
-    t.L = second ? b.L : a.L;
-    t.h = second ? b.h : a.h;
-    return t;
 }
 
 // Per-row gate inputs of a tile, loaded one pair ahead and kept raw (no
@@ -633,44 +714,62 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 : 0;
 
     if (warp == kProducerWarp) {
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
-                         : "memory");
+        // Lanes 0 and 1 walk the two tiles of pair q (loaded into the stage ring),
+        // lanes 2 and 3 those of pair q + kPrefetchPairs (prefetched into L2).
+        // Each lane issues the copies of its own tile, so one warp instruction
+        // covers all four; lane 0 owns the stage barriers.
+        if (lane < 4) {
+            if (lane == 0)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
+                             : "memory");
+            const int tt = lane & 1;
+            const bool pf_lane = lane >= 2;
+            TileWalk w = walk_init(p, static_cast<uint32_t>(2 * blockIdx.x + tt));
+            if (pf_lane)
+                for (int i = 0; i < kPrefetchPairs; ++i) walk_advance(p, w, p.pair_ds, p.pair_dh);
             int64_t q = 0;
             for (; q < n_local; ++q) {
-                if (*abort_flag) break;
+                int stop = (lane == 0) ? *abort_flag : 0;
+                if (__shfl_sync(0xFu, stop, 0)) break;
+                const Tile t = walk_tile(p, w);
+                if (pf_lane) {
+                    if (q + kPrefetchPairs < n_local) {
+                        if (t.L > 0) {
+                            tma_prefetch_3d(&tmap_k, 0, t.h, static_cast<int>(t.row0));
+                            tma_prefetch_3d(&tmap_k, 64, t.h, static_cast<int>(t.row0));
+                        }
+                        walk_advance(p, w, p.pair_ds, p.pair_dh);
+                    }
+                } else if (q + 1 < n_local) {
+                    walk_advance(p, w, p.pair_ds, p.pair_dh);
+                }
+                const uint32_t loads = __ballot_sync(0xFu, !pf_lane && t.L > 0) & 3u;
                 const int s = static_cast<int>(q % kNumStages);
                 const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
-                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
-                    record_timeout(p, abort_flag);
-                    break;
-                }
-                const int64_t pair = blockIdx.x + q * gridDim.x;
-                const Tile t0 = tile_of(p, 2 * pair);
-                const Tile t1 = tile_of(p, 2 * pair + 1);
-                const uint32_t bytes = (t0.L > 0 ? 2 * kBoxBytes : 0) + (t1.L > 0 ? 2 * kBoxBytes : 0);
                 const uint32_t st = sbase + kOffK + s * kStageBytes;
-                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
-                if (t0.L > 0) {
-                    tma_load_3d(st + 0 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t0.h,
-                                static_cast<int>(t0.row0));
-                    tma_load_3d(st + 2 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t0.h,
-                                static_cast<int>(t0.row0));
+                int ok = 1;
+                if (lane == 0) {
+                    ok = mbar_wait(bar_empty + 8 * s, ph ^ 1) ? 1 : 0;
+                    if (!ok) record_timeout(p, abort_flag);
+                    else mbar_arrive_expect_tx(bar_full + 8 * s, __popc(loads) * 2 * kBoxBytes);
                 }
-                if (t1.L > 0) {
-                    tma_load_3d(st + 1 * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t1.h,
-                                static_cast<int>(t1.row0));
-                    tma_load_3d(st + 3 * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t1.h,
-                                static_cast<int>(t1.row0));
+                if (!__shfl_sync(0xFu, ok, 0)) break;
+                if (!pf_lane && t.L > 0) {
+                    tma_load_3d(st + tt * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t.h,
+                                static_cast<int>(t.row0));
+                    tma_load_3d(st + (2 + tt) * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t.h,
+                                static_cast<int>(t.row0));
                 }
             }
-            // Drain: every issued load has landed and every stage's MMAs committed.
-            const int64_t first = q > kNumStages ? q - kNumStages : 0;
-            for (int64_t r = first; r < q; ++r) {
-                const int s = static_cast<int>(r % kNumStages);
-                const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
-                if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
-                if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
+            if (lane == 0) {
+                // Drain: every issued load has landed and every stage's MMAs committed.
+                const int64_t first = q > kNumStages ? q - kNumStages : 0;
+                for (int64_t r = first; r < q; ++r) {
+                    const int s = static_cast<int>(r % kNumStages);
+                    const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
+                    if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
+                    if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -688,16 +787,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t st = sbase + kOffK + s * kStageBytes;
-#pragma unroll
-                for (int bt = 0; bt < 2; ++bt) {
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w + 64 * bt);
+                {
+                    // One N = 128 product per K step: rows and columns both run over
+                    // the pair's 128 key rows; each tile reads its own diagonal block.
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w);
 #pragma unroll
                     for (int kh = 0; kh < 2; ++kh) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
-                            const uint32_t b_addr = a_addr + bt * kBoxBytes;
-                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(b_addr), kIdesc,
+                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(a_addr), kIdesc,
                                        (kh | ks) ? 1u : 0u);
                         }
                     }
@@ -730,25 +829,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int bar_id = 1 + wg;
 
         int64_t q = wg;
-        Tile cur0 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x));
-        Tile cur1 = tile_of(p, 2 * (blockIdx.x + q * gridDim.x) + 1);
-        RowIn rin = load_row(p, pick(cur0, cur1, tt_e), i_e);
+        // This thread's tile (tt_e) of each of the warpgroup's pairs.
+        TileWalk wk = walk_init(p, static_cast<uint32_t>(2 * (blockIdx.x + q * gridDim.x) + tt_e));
+        Tile cur = walk_tile(p, wk);
+        RowIn rin = load_row(p, cur, i_e);
 
         for (int r = 0; q < n_local; ++r, q += kNumWG) {
             // Prefetch the next pair's schedule and row inputs.
             const int64_t qn = q + kNumWG;
-            Tile nx0, nx1;
-            nx0.L = nx1.L = 0;
-            nx0.row0 = nx1.row0 = 0;
-            nx0.h = nx1.h = 0;
+            Tile nx;
+            nx.L = 0;
+            nx.row0 = 0;
+            nx.h = 0;
             if (qn < n_local) {
-                nx0 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x));
-                nx1 = tile_of(p, 2 * (blockIdx.x + qn * gridDim.x) + 1);
+                walk_advance(p, wk, p.wg_ds, p.wg_dh);
+                nx = walk_tile(p, wk);
             }
-            const RowIn rnext = load_row(p, pick(nx0, nx1, tt_e), i_e);
+            const RowIn rnext = load_row(p, nx, i_e);
 
-            if (qd == 0 && lane == 0) {
-                bulk_wait_read();
+            if ((qd & 1) == 0 && lane == 0) bulk_wait_read();   // this warp's previous store
+            if (qd == 3 && lane == 0) {
                 int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
                 wg_flag[wg] = ok;
@@ -758,7 +858,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // only when every |g - gref| <= 30 in both tiles (no overflow, and
             // the [-50, 50] clamp cannot bind); otherwise the clamped
             // exp(g_i - g_j) is evaluated directly.
-            const Tile te = pick(cur0, cur1, tt_e);
+            const Tile te = cur;
             const bool rowok = i_e < te.L;
             float ui = 1.0f, vi = 1.0f;
             bool unsafe = false;
@@ -885,23 +985,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             named_bar_sync(bar_id, 128);                       // B5: X complete
 
             // ---- store: full chunks by TMA from the staging, partial chunks row by row
-            if (tid == 0) {
-                bool any = false;
-#pragma unroll
-                for (int t2 = 0; t2 < 2; ++t2) {
-                    const Tile ts = pick(cur0, cur1, t2);
-                    if (ts.L == kChunk) {
-                        const uint32_t src = smem_u32(abuf + (t2 ? kStage1Off : 0));
-                        tma_store_3d(&tmap_out, src, 0, ts.h, static_cast<int>(ts.row0));
-                        if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, ts.h, static_cast<int>(ts.row0));
-                        any = true;
-                    }
-                }
-                if (any) bulk_commit();
+            // Lane 0 of warps 0 and 2 stores the tile its warp's rows belong to.
+            if (lane == 0 && (qd & 1) == 0 && cur.L == kChunk) {
+                const uint32_t src = smem_u32(abuf + (tt_e ? kStage1Off : 0));
+                tma_store_3d(&tmap_out, src, 0, cur.h, static_cast<int>(cur.row0));
+                if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, cur.h, static_cast<int>(cur.row0));
+                bulk_commit();
             }
             {
-                const int st_t = qd >> 1;
-                const Tile ts = pick(cur0, cur1, st_t);
+                const int st_t = tt_e;
+                const Tile ts = cur;
                 if (ts.L > 0 && ts.L < kChunk) {
                     const uint8_t *sb = abuf + (st_t ? kStage1Off : 0);
                     constexpr int kPieces = OUT_BF16 ? 8 : 16;
@@ -919,11 +1012,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            cur0 = nx0;
-            cur1 = nx1;
+            cur = nx;
             rin = rnext;
         }
-        if (tid == 0) bulk_wait_all();
+        if (lane == 0 && (qd & 1) == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -1079,6 +1171,10 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
     prm.status = status_ptr;
 
     const int64_t grid = prm.n_pairs < sms ? prm.n_pairs : sms;
+    prm.pair_ds = static_cast<uint32_t>((2 * grid) / H);
+    prm.pair_dh = static_cast<uint32_t>((2 * grid) % H);
+    prm.wg_ds = static_cast<uint32_t>((2 * grid * kNumWG) / H);
+    prm.wg_dh = static_cast<uint32_t>((2 * grid * kNumWG) % H);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (out_dtype == GDR_BF16)
         kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
