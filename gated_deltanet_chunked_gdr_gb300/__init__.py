@@ -29,9 +29,10 @@ GDR_ERR_CUDA = -7
 GDR_ERR_TIMEOUT = -8
 GDR_F32 = 0
 GDR_BF16 = 1
+GDR_F16 = 2
 
-EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_status_string", "gdr_kkt_solve_device_status",
-                    "gdr_kkt_solve_num_sms")
+EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_kkt_solve_ex", "gdr_status_string",
+                    "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms")
 
 _lib = None
 _lock = threading.Lock()
@@ -63,6 +64,8 @@ def load_library():
             vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
             lib.gdr_kkt_solve.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp, vp]
             lib.gdr_kkt_solve.restype = ci
+            lib.gdr_kkt_solve_ex.argtypes = [vp, ci, vp, vp, ci, vp, i64, i64, i64, i64, ci, ci, vp, vp]
+            lib.gdr_kkt_solve_ex.restype = ci
             lib.gdr_status_string.argtypes = [ci]
             lib.gdr_status_string.restype = ctypes.c_char_p
             lib.gdr_kkt_solve_device_status.argtypes = [ctypes.POINTER(ci)]
@@ -85,6 +88,24 @@ def kkt_solve_raw(k_ptr: int, g_ptr: int, beta_ptr: int, cu_ptr: int, B: int, T:
                                         out_ptr or None, stream or None)
 
 
+def kkt_solve_ex_raw(k_ptr: int, k_dtype: int, g_ptr: int, beta_ptr: int, beta_dtype: int,
+                     cu_ptr: int, B: int, T: int, H: int, K: int, chunk_size: int,
+                     out_dtype: int, out_ptr: int, stream: int) -> int:
+    """Direct call of gdr_kkt_solve_ex with integer pointers; returns the gdr_status code."""
+    return load_library().gdr_kkt_solve_ex(k_ptr or None, k_dtype, g_ptr or None, beta_ptr or None,
+                                           beta_dtype, cu_ptr or None, B, T, H, K, chunk_size,
+                                           out_dtype, out_ptr or None, stream or None)
+
+
+def _gdr_dtype(dt, what: str) -> int:
+    import torch
+
+    table = {torch.float32: GDR_F32, torch.bfloat16: GDR_BF16, torch.float16: GDR_F16}
+    if dt not in table:
+        raise TypeError(f"{what} must be torch.float32, torch.bfloat16 or torch.float16")
+    return table[dt]
+
+
 def device_status() -> int:
     """Reads and clears the device-side status word (synchronises the device)."""
     v = ctypes.c_int(0)
@@ -105,24 +126,27 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
               out=None, stream=None):
     """(I + A)^{-1} of every 64-token chunk and head, on the GPU.
 
-    k: bf16 [B, T, H, 128] CUDA tensor ([1, T, H, 128] with cu_seqlens);
-    g: fp32 [B, T, H] or None; beta: bf16 [B, T, H] or None;
-    cu_seqlens: int32 [N + 1] CUDA tensor or None; output_dtype: torch.float32
-    (default) or torch.bfloat16.  Returns out [B, T, H, 64]."""
+    k: bf16 or fp16 [B, T, H, K] CUDA tensor, K in {64, 128, 192, 256}
+    ([1, T, H, K] with cu_seqlens); g: fp32 [B, T, H] or None; beta: fp32,
+    bf16 or fp16 [B, T, H] or None; cu_seqlens: int32 [N + 1] CUDA tensor or
+    None; output_dtype: torch.float32 (default), torch.bfloat16 or
+    torch.float16.  Returns out [B, T, H, 64]."""
     import torch
 
     if chunk_size != 64:
         raise ValueError("chunk_size must be 64")
     if output_dtype is None:
         output_dtype = torch.float32
-    if output_dtype not in (torch.float32, torch.bfloat16):
-        raise TypeError("output_dtype must be torch.float32 or torch.bfloat16")
-    if k.dtype != torch.bfloat16 or k.dim() != 4 or not k.is_cuda:
-        raise TypeError("k must be a 4-D bf16 CUDA tensor")
-    for name, t, dt in (("g", g, torch.float32), ("beta", beta, torch.bfloat16),
-                        ("cu_seqlens", cu_seqlens, torch.int32)):
+    out_code = _gdr_dtype(output_dtype, "output_dtype")
+    if k.dtype not in (torch.bfloat16, torch.float16) or k.dim() != 4 or not k.is_cuda:
+        raise TypeError("k must be a 4-D bf16 or fp16 CUDA tensor")
+    k_code = _gdr_dtype(k.dtype, "k")
+    beta_code = GDR_F32 if beta is None else _gdr_dtype(beta.dtype, "beta")
+    for name, t, dt in (("g", g, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)):
         if t is not None and (t.dtype != dt or t.device != k.device):
             raise TypeError(f"{name} must be a {dt} tensor on {k.device}")
+    if beta is not None and beta.device != k.device:
+        raise TypeError(f"beta must be on {k.device}")
     Bk, T, H, K = k.shape
     if cu_seqlens is not None:
         if Bk != 1 or cu_seqlens.dim() != 1:
@@ -144,16 +168,14 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
     if stream is None:
         stream = torch.cuda.current_stream(k.device).cuda_stream
     with torch.cuda.device(k.device):
-        rc = kkt_solve_raw(k.data_ptr(), 0 if g is None else g.data_ptr(),
-                           0 if beta is None else beta.data_ptr(),
-                           0 if cu_seqlens is None else cu_seqlens.data_ptr(),
-                           B, T, H, K, chunk_size,
-                           GDR_BF16 if output_dtype == torch.bfloat16 else GDR_F32,
-                           out.data_ptr(), int(stream))
+        rc = kkt_solve_ex_raw(k.data_ptr(), k_code, 0 if g is None else g.data_ptr(),
+                              0 if beta is None else beta.data_ptr(), beta_code,
+                              0 if cu_seqlens is None else cu_seqlens.data_ptr(),
+                              B, T, H, K, chunk_size, out_code, out.data_ptr(), int(stream))
     if rc != GDR_OK:
-        raise GdrError(rc, "gdr_kkt_solve")
+        raise GdrError(rc, "gdr_kkt_solve_ex")
     return out
 
 
-__all__ = ["kkt_solve", "kkt_solve_raw", "device_status", "num_sms", "build", "load_library",
+__all__ = ["kkt_solve", "kkt_solve_raw", "kkt_solve_ex_raw", "device_status", "num_sms", "build", "load_library",
            "status_string", "GdrError", "EXPORTED_SYMBOLS"]

@@ -36,6 +36,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -48,7 +49,7 @@
 namespace gdr {
 
 constexpr int kChunk = 64;
-constexpr int kHeadK = 128;
+constexpr int kMaxHeadK = 256;                    // K = 64, 128, 192 or 256
 constexpr int kNumWG = 3;
 constexpr int kNumStages = 3;
 constexpr int kNumConsumerWarps = 4 * kNumWG;
@@ -107,7 +108,7 @@ inline FastDiv make_fastdiv(uint32_t d) {
 
 struct Params {
     const float *g;
-    const __nv_bfloat16 *beta;
+    const void *beta;
     const int32_t *cu;
     void *out;
     int64_t B, T, H;
@@ -119,6 +120,8 @@ struct Params {
     uint32_t pair_ds, pair_dh;   // stride between a CTA's consecutive pairs (2 * grid tiles) as (slots, heads)
     uint32_t wg_ds, wg_dh;       // stride between a warpgroup's consecutive pairs (2 * grid * warpgroups tiles)
     int *status;
+    uint32_t idesc;    // tcgen05 instruction descriptor for the key type
+    int beta_kind;     // gdr_dtype of beta (GDR_F32 when beta is NULL)
 };
 
 struct Tile {
@@ -250,9 +253,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(2) << 61;
     return d;
 }
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N=128, M=128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
-                            ((128u >> 4) << 24);
+// Instruction descriptor, kind::f16: D fp32, A and B of the key type (format 1 =
+// bf16, 0 = fp16), both K-major, N = 128, M = 128.
+constexpr uint32_t idesc_f16_kind(bool bf16_keys) {
+    return (1u << 4) | ((bf16_keys ? 1u : 0u) << 7) | ((bf16_keys ? 1u : 0u) << 10) |
+           ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
 
 // ------------------------------------------------------------ tile schedule
 // Tile u = slot * H + h.  Fixed-length: slot = b * NT + c.  Varlen: sequence n
@@ -512,37 +518,41 @@ __device__ __forceinline__ void merge_column(const float *At, int g, int t,
 // X is assembled in the layout a 128-byte-swizzled TMA store reads: a tile's 64
 // rows of 128 bytes (bf16: 64 values; fp32: two 32-value halves 8 KB apart), the
 // 16-byte piece q of row r stored at piece position q ^ (r % 8).
-template <bool BF16>
+template <bool OUT16>
 __device__ __forceinline__ uint32_t stage_piece_off(int r, int q) {
-    if (BF16) return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
+    if (OUT16) return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
     return static_cast<uint32_t>((q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4));
 }
 
-template <bool BF16>
-__device__ __forceinline__ void stage_put(uint8_t *st, int r, int c, float v) {
-    if (BF16) {
-        *reinterpret_cast<__nv_bfloat16 *>(st + stage_piece_off<true>(r, c >> 3) + 2 * (c & 7)) =
-            __float2bfloat16_rn(v);
-    } else {
-        *reinterpret_cast<float *>(st + stage_piece_off<false>(r, c >> 2) + 4 * (c & 3)) = v;
-    }
+// One fp32 value of X at (r, c) in the fp32 staging.
+__device__ __forceinline__ void stage_put_f32(uint8_t *st, int r, int c, float v) {
+    *reinterpret_cast<float *>(st + stage_piece_off<false>(r, c >> 2) + 4 * (c & 3)) = v;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+// Output kinds (the gdr_dtype values): fp32, bf16, fp16.  The 16-bit kinds share
+// the staging layout and differ only in the rounding to 16 bits (both
+// round-to-nearest-even); a holds the lower column.
+constexpr int kOutF32 = 0, kOutBF16 = 1, kOutF16 = 2;
+template <int OUT>
+__device__ __forceinline__ uint32_t pack16x2(float a, float b) {
+    if (OUT == kOutF16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
 // Row r of X restricted to columns >= 16 I: the diagonal block row (d[0..3] =
 // 16 values) followed by zeros.
-template <bool BF16>
+template <int OUT>
 __device__ __forceinline__ void stage_diag_row(uint8_t *st, int r, int I, const float4 (&d)[4]) {
-    if (BF16) {
+    if (OUT != kOutF32) {
         uint4 a, b;
-        a.x = pack_bf16x2(d[0].x, d[0].y); a.y = pack_bf16x2(d[0].z, d[0].w);
-        a.z = pack_bf16x2(d[1].x, d[1].y); a.w = pack_bf16x2(d[1].z, d[1].w);
-        b.x = pack_bf16x2(d[2].x, d[2].y); b.y = pack_bf16x2(d[2].z, d[2].w);
-        b.z = pack_bf16x2(d[3].x, d[3].y); b.w = pack_bf16x2(d[3].z, d[3].w);
+        a.x = pack16x2<OUT>(d[0].x, d[0].y); a.y = pack16x2<OUT>(d[0].z, d[0].w);
+        a.z = pack16x2<OUT>(d[1].x, d[1].y); a.w = pack16x2<OUT>(d[1].z, d[1].w);
+        b.x = pack16x2<OUT>(d[2].x, d[2].y); b.y = pack16x2<OUT>(d[2].z, d[2].w);
+        b.z = pack16x2<OUT>(d[3].x, d[3].y); b.w = pack16x2<OUT>(d[3].z, d[3].w);
         *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I)) = a;
         *reinterpret_cast<uint4 *>(st + stage_piece_off<true>(r, 2 * I + 1)) = b;
 #pragma unroll
@@ -560,7 +570,7 @@ __device__ __forceinline__ void stage_diag_row(uint8_t *st, int r, int I, const 
 }
 
 // Z_JI (accumulator layout) -> rows 16I.. / columns 16J.. of X in the staging.
-// bf16: one transposing matrix store; the accumulator pairs (z[nt][0], z[nt][1])
+// 16-bit output: one transposing matrix store; the accumulator pairs (z[nt][0], z[nt][1])
 // and (z[nt][2], z[nt][3]) are the fragments of four 8x8 matrices, stored
 // transposed, whose rows (X rows 16I + 8 (m / 2) + b, 16-byte piece 2J + m % 2)
 // are addressed by lane 8m + b.
@@ -570,22 +580,22 @@ __device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, ui
                  "r"(r0), "r"(r1), "r"(r2), "r"(r3)
                  : "memory");
 }
-template <bool BF16>
+template <int OUT>
 __device__ __forceinline__ void stage_block_T(uint8_t *st, int I, int J, const float (&z)[2][4],
                                               int g, int t) {
-    if (BF16) {
+    if (OUT != kOutF32) {
         const int lane = 4 * g + t, m = lane >> 3, b = lane & 7;
         const uint32_t addr = smem_u32(st + stage_piece_off<true>(16 * I + 8 * (m >> 1) + b, 2 * J + (m & 1)));
-        stmatrix_x4_trans(addr, pack_bf16x2(z[0][0], z[0][1]), pack_bf16x2(z[0][2], z[0][3]),
-                          pack_bf16x2(z[1][0], z[1][1]), pack_bf16x2(z[1][2], z[1][3]));
+        stmatrix_x4_trans(addr, pack16x2<OUT>(z[0][0], z[0][1]), pack16x2<OUT>(z[0][2], z[0][3]),
+                          pack16x2<OUT>(z[1][0], z[1][1]), pack16x2<OUT>(z[1][2], z[1][3]));
     } else {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int r0 = 16 * I + 8 * nt + 2 * t, c0 = 16 * J + g;
-            stage_put<false>(st, r0, c0, z[nt][0]);
-            stage_put<false>(st, r0 + 1, c0, z[nt][1]);
-            stage_put<false>(st, r0, c0 + 8, z[nt][2]);
-            stage_put<false>(st, r0 + 1, c0 + 8, z[nt][3]);
+            stage_put_f32(st, r0, c0, z[nt][0]);
+            stage_put_f32(st, r0 + 1, c0, z[nt][1]);
+            stage_put_f32(st, r0, c0 + 8, z[nt][2]);
+            stage_put_f32(st, r0 + 1, c0 + 8, z[nt][3]);
         }
     }
 }
@@ -629,7 +639,7 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
 // row's g and beta, and the chunk's first and last g.
 struct RowIn {
     float g, gfirst, glast;
-    unsigned short beta;   // bf16 bits
+    uint32_t beta;     // raw bits of beta in its own type
 };
 
 __device__ __forceinline__ RowIn load_row(const Params &p, const Tile &t, int i) {
@@ -637,7 +647,7 @@ __device__ __forceinline__ RowIn load_row(const Params &p, const Tile &t, int i)
     r.g = 0.0f;
     r.gfirst = 0.0f;
     r.glast = 0.0f;
-    r.beta = 0;
+    r.beta = 0x3F800000u;   // fp32 1.0 (beta NULL is read as fp32)
     if (i < t.L) {
         const int64_t base = t.row0 * p.H + t.h;
         if (p.g) {
@@ -645,15 +655,20 @@ __device__ __forceinline__ RowIn load_row(const Params &p, const Tile &t, int i)
             r.gfirst = __ldg(p.g + base);
             r.glast = __ldg(p.g + base + static_cast<int64_t>(t.L - 1) * p.H);
         }
-        r.beta = p.beta ? __ldg(reinterpret_cast<const unsigned short *>(p.beta) + base +
-                                static_cast<int64_t>(i) * p.H)
-                        : static_cast<unsigned short>(0x3F80);   // bf16 1.0
+        if (p.beta) {
+            const int64_t at = base + static_cast<int64_t>(i) * p.H;
+            r.beta = p.beta_kind == GDR_F32
+                         ? __ldg(reinterpret_cast<const uint32_t *>(p.beta) + at)
+                         : static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(p.beta) + at));
+        }
     }
     return r;
 }
 
-__device__ __forceinline__ float bf16_bits_to_float(unsigned short b) {
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+__device__ __forceinline__ float beta_value(const Params &p, uint32_t bits) {
+    if (p.beta_kind == GDR_BF16) return __uint_as_float(bits << 16);
+    if (p.beta_kind == GDR_F16) return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+    return __uint_as_float(bits);
 }
 
 __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred) {
@@ -669,7 +684,11 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
     return out != 0;
 }
 
-template <bool OUT_BF16>
+// OUT: kOutF32, kOutBF16 or kOutF16.  The merge runs split (fp32-accurate) for
+// fp32 and fp16 output and as one tf32 pass for bf16 output.  NKB = K / 64, the
+// 64-column key boxes per row; it only shapes the producer and MMA loops, which
+// sit on the pipeline's critical path and so are fully unrolled per K.
+template <int OUT, int NKB>
 __global__ void __launch_bounds__(kNumThreads, 1)
     kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_out, const Params p) {
@@ -713,6 +732,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
                                 : 0;
 
+    // The pipeline unit is (pair, 128-column chunk of K): K = 64 or 128 takes one
+    // unit per pair, K = 192 or 256 two.  A unit holds one or two 64-column boxes
+    // of each of the pair's tiles; the Gram accumulates over a pair's units.
+    constexpr int nkb = NKB;
+    constexpr int nkc = (nkb + 1) >> 1;
     if (warp == kProducerWarp) {
         // Lanes 0 and 1 walk the two tiles of pair q (loaded into the stage ring),
         // lanes 2 and 3 those of pair q + kPrefetchPairs (prefetched into L2).
@@ -728,43 +752,54 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (pf_lane)
                 for (int i = 0; i < kPrefetchPairs; ++i) walk_advance(p, w, p.pair_ds, p.pair_dh);
             int64_t q = 0;
+            int kc = 0;             // units of pair q issued when the loop stops inside it
+            bool failed = false;
             for (; q < n_local; ++q) {
                 int stop = (lane == 0) ? *abort_flag : 0;
                 if (__shfl_sync(0xFu, stop, 0)) break;
                 const Tile t = walk_tile(p, w);
                 if (pf_lane) {
                     if (q + kPrefetchPairs < n_local) {
-                        if (t.L > 0) {
-                            tma_prefetch_3d(&tmap_k, 0, t.h, static_cast<int>(t.row0));
-                            tma_prefetch_3d(&tmap_k, 64, t.h, static_cast<int>(t.row0));
-                        }
+                        if (t.L > 0)
+#pragma unroll
+                            for (int kb = 0; kb < nkb; ++kb)
+                                tma_prefetch_3d(&tmap_k, 64 * kb, t.h, static_cast<int>(t.row0));
                         walk_advance(p, w, p.pair_ds, p.pair_dh);
                     }
                 } else if (q + 1 < n_local) {
                     walk_advance(p, w, p.pair_ds, p.pair_dh);
                 }
                 const uint32_t loads = __ballot_sync(0xFu, !pf_lane && t.L > 0) & 3u;
-                const int s = static_cast<int>(q % kNumStages);
-                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
-                const uint32_t st = sbase + kOffK + s * kStageBytes;
-                int ok = 1;
-                if (lane == 0) {
-                    ok = mbar_wait(bar_empty + 8 * s, ph ^ 1) ? 1 : 0;
-                    if (!ok) record_timeout(p, abort_flag);
-                    else mbar_arrive_expect_tx(bar_full + 8 * s, __popc(loads) * 2 * kBoxBytes);
+#pragma unroll
+                for (kc = 0; kc < nkc; ++kc) {
+                    const int64_t v = q * nkc + kc;
+                    const int nb = (2 * kc + 1 < nkb) ? 2 : 1;
+                    const int s = static_cast<int>(v % kNumStages);
+                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                    const uint32_t st = sbase + kOffK + s * kStageBytes;
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = mbar_wait(bar_empty + 8 * s, ph ^ 1) ? 1 : 0;
+                        if (!ok) record_timeout(p, abort_flag);
+                        else mbar_arrive_expect_tx(bar_full + 8 * s, __popc(loads) * nb * kBoxBytes);
+                    }
+                    if (!__shfl_sync(0xFu, ok, 0)) {
+                        failed = true;
+                        break;
+                    }
+                    if (!pf_lane && t.L > 0)
+#pragma unroll
+                        for (int kh = 0; kh < nb; ++kh)
+                            tma_load_3d(st + (2 * kh + tt) * kBoxBytes, &tmap_k, bar_full + 8 * s,
+                                        64 * (2 * kc + kh), t.h, static_cast<int>(t.row0));
                 }
-                if (!__shfl_sync(0xFu, ok, 0)) break;
-                if (!pf_lane && t.L > 0) {
-                    tma_load_3d(st + tt * kBoxBytes, &tmap_k, bar_full + 8 * s, 0, t.h,
-                                static_cast<int>(t.row0));
-                    tma_load_3d(st + (2 + tt) * kBoxBytes, &tmap_k, bar_full + 8 * s, 64, t.h,
-                                static_cast<int>(t.row0));
-                }
+                if (failed) break;
             }
+            const int64_t v = q * nkc + (failed ? kc : 0);   // units issued
             if (lane == 0) {
                 // Drain: every issued load has landed and every stage's MMAs committed.
-                const int64_t first = q > kNumStages ? q - kNumStages : 0;
-                for (int64_t r = first; r < q; ++r) {
+                const int64_t first = v > kNumStages ? v - kNumStages : 0;
+                for (int64_t r = first; r < v; ++r) {
                     const int s = static_cast<int>(r % kNumStages);
                     const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
                     if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
@@ -774,35 +809,42 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            int64_t q = 0;
+            int64_t q = 0;          // ends as the number of pairs whose Gram was committed
+            bool failed = false;
             for (; q < n_local; ++q) {
                 if (*abort_flag) break;
-                const int s = static_cast<int>(q % kNumStages);
-                const uint32_t ph = static_cast<uint32_t>((q / kNumStages) & 1);
                 const int w = static_cast<int>(q % kNumWG);
                 const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
-                if (!mbar_wait(bar_full + 8 * s, ph) || !mbar_wait(bar_tempty + 8 * w, phw ^ 1)) {
-                    record_timeout(p, abort_flag);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t st = sbase + kOffK + s * kStageBytes;
-                {
+                const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w);
+#pragma unroll
+                for (int kc = 0; kc < nkc; ++kc) {
+                    const int64_t v = q * nkc + kc;
+                    const int s = static_cast<int>(v % kNumStages);
+                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                    if (!mbar_wait(bar_full + 8 * s, ph) ||
+                        (kc == 0 && !mbar_wait(bar_tempty + 8 * w, phw ^ 1))) {
+                        record_timeout(p, abort_flag);
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
                     // One N = 128 product per K step: rows and columns both run over
                     // the pair's 128 key rows; each tile reads its own diagonal block.
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w);
+                    const uint32_t st = sbase + kOffK + s * kStageBytes;
+                    const int nb = (2 * kc + 1 < nkb) ? 2 : 1;
 #pragma unroll
-                    for (int kh = 0; kh < 2; ++kh) {
+                    for (int kh = 0; kh < nb; ++kh) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
-                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(a_addr), kIdesc,
-                                       (kh | ks) ? 1u : 0u);
+                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(a_addr), p.idesc,
+                                       (kc | kh | ks) ? 1u : 0u);
                         }
                     }
+                    tc_commit(bar_empty + 8 * s);
+                    if (kc == nkc - 1) tc_commit(bar_tfull + 8 * w);
                 }
-                tc_commit(bar_empty + 8 * s);
-                tc_commit(bar_tfull + 8 * w);
+                if (failed) break;
             }
             // The last pair's MMAs must be complete before TMEM is released.
             if (q > 0) {
@@ -903,7 +945,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     for (int j4 = 0; j4 < 16; ++j4)
                         if (j4 < n4) Arow[j4] = z;
                 } else if (!direct) {
-                    const float w = bf16_bits_to_float(rin.beta) * ui;
+                    const float w = beta_value(p, rin.beta) * ui;
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
@@ -917,7 +959,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                     }
                 } else {
-                    const float gi = rin.g, bi = bf16_bits_to_float(rin.beta);
+                    const float gi = rin.g, bi = beta_value(p, rin.beta);
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4) {
                         if (j4 < n4) {
@@ -960,26 +1002,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
             if (qd < 2) {
                 float z0[3][2][4];
-                merge_column<0, !OUT_BF16>(At(mt), g8, t4, z0);
+                merge_column<0, OUT != kOutBF16>(At(mt), g8, t4, z0);
                 named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                stage_block_T<OUT_BF16>(st_m, 1, 0, z0[0], g8, t4);
-                stage_block_T<OUT_BF16>(st_m, 2, 0, z0[1], g8, t4);
-                stage_block_T<OUT_BF16>(st_m, 3, 0, z0[2], g8, t4);
+                stage_block_T<OUT>(st_m, 1, 0, z0[0], g8, t4);
+                stage_block_T<OUT>(st_m, 2, 0, z0[1], g8, t4);
+                stage_block_T<OUT>(st_m, 3, 0, z0[2], g8, t4);
             } else {
                 float z1[2][2][4], z2[1][2][4];
-                merge_column<1, !OUT_BF16>(At(mt), g8, t4, z1);
-                merge_column<2, !OUT_BF16>(At(mt), g8, t4, z2);
+                merge_column<1, OUT != kOutBF16>(At(mt), g8, t4, z1);
+                merge_column<2, OUT != kOutBF16>(At(mt), g8, t4, z2);
                 named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                stage_block_T<OUT_BF16>(st_m, 2, 1, z1[0], g8, t4);
-                stage_block_T<OUT_BF16>(st_m, 3, 1, z1[1], g8, t4);
-                stage_block_T<OUT_BF16>(st_m, 3, 2, z2[0], g8, t4);
+                stage_block_T<OUT>(st_m, 2, 1, z1[0], g8, t4);
+                stage_block_T<OUT>(st_m, 3, 1, z1[1], g8, t4);
+                stage_block_T<OUT>(st_m, 3, 2, z2[0], g8, t4);
             }
             {
                 const float4 dv[4] = {make_float4(drow[0], drow[1], drow[2], drow[3]),
                                       make_float4(drow[4], drow[5], drow[6], drow[7]),
                                       make_float4(drow[8], drow[9], drow[10], drow[11]),
                                       make_float4(drow[12], drow[13], drow[14], drow[15])};
-                stage_diag_row<OUT_BF16>(abuf + (dt ? kStage1Off : 0), 16 * dI + dc, dI, dv);
+                stage_diag_row<OUT>(abuf + (dt ? kStage1Off : 0), 16 * dI + dc, dI, dv);
             }
             fence_proxy_async_smem();
             named_bar_sync(bar_id, 128);                       // B5: X complete
@@ -989,7 +1031,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (lane == 0 && (qd & 1) == 0 && cur.L == kChunk) {
                 const uint32_t src = smem_u32(abuf + (tt_e ? kStage1Off : 0));
                 tma_store_3d(&tmap_out, src, 0, cur.h, static_cast<int>(cur.row0));
-                if (!OUT_BF16) tma_store_3d(&tmap_out, src + 8192, 32, cur.h, static_cast<int>(cur.row0));
+                if (OUT == kOutF32) tma_store_3d(&tmap_out, src + 8192, 32, cur.h, static_cast<int>(cur.row0));
                 bulk_commit();
             }
             {
@@ -997,17 +1039,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const Tile ts = cur;
                 if (ts.L > 0 && ts.L < kChunk) {
                     const uint8_t *sb = abuf + (st_t ? kStage1Off : 0);
-                    constexpr int kPieces = OUT_BF16 ? 8 : 16;
+                    constexpr int kPieces = OUT != kOutF32 ? 8 : 16;
                     constexpr int kRowsPerIt = 32 / kPieces;
 #pragma unroll 2
                     for (int it = 0; it < 32 / kRowsPerIt; ++it) {
                         const int rr = 32 * (qd & 1) + kRowsPerIt * it + lane / kPieces;
                         const int piece = lane % kPieces;
                         if (rr < ts.L) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(sb + stage_piece_off<OUT_BF16>(rr, piece));
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sb + stage_piece_off<OUT != kOutF32>(rr, piece));
                             const int64_t orow = (ts.row0 + rr) * p.H + ts.h;
                             *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) +
-                                                       orow * (OUT_BF16 ? 128 : 256) + 16 * piece) = v;
+                                                       orow * (OUT != kOutF32 ? 128 : 256) + 16 * piece) = v;
                         }
                     }
                 }
@@ -1041,6 +1083,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+using KernelFn = void (*)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap, Params);
+
+template <int OUT>
+KernelFn kernel_for_nkb(int nkb) {
+    switch (nkb) {
+        case 1: return kkt_solve_kernel<OUT, 1>;
+        case 2: return kkt_solve_kernel<OUT, 2>;
+        case 3: return kkt_solve_kernel<OUT, 3>;
+        default: return kkt_solve_kernel<OUT, 4>;
+    }
+}
+
+// The instantiation for an output kind (gdr_dtype value) and K / 64.
+KernelFn kernel_for(int out_kind, int nkb) {
+    if (out_kind == kOutBF16) return kernel_for_nkb<kOutBF16>(nkb);
+    if (out_kind == kOutF16) return kernel_for_nkb<kOutF16>(nkb);
+    return kernel_for_nkb<kOutF32>(nkb);
+}
+
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_ready[kMaxDevices];   // 0 unknown, 1 ready, -1 unsupported
 std::atomic<int> g_dev_sms[kMaxDevices];
@@ -1064,10 +1125,12 @@ int prepare_device(int *sms) {
             g_dev_ready[dev].store(-1, std::memory_order_release);
             return GDR_ERR_DEVICE;
         }
-        if (cudaFuncSetAttribute(kkt_solve_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(kkt_solve_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess) {
+        bool attr_ok = true;
+        for (int o = 0; o < 3; ++o)
+            for (int n = 1; n <= 4; ++n)
+                attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(o, n), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                          kSmemBytes) == cudaSuccess;
+        if (!attr_ok) {
             cudaGetLastError();
             return GDR_ERR_CUDA;
         }
@@ -1088,9 +1151,9 @@ const char *gdr_status_string(int status) {
     switch (status) {
         case GDR_OK: return "ok";
         case GDR_ERR_NULL: return "a required pointer is NULL";
-        case GDR_ERR_SHAPE: return "unsupported or inconsistent sizes (K must be 128; B*T < 2^31)";
+        case GDR_ERR_SHAPE: return "unsupported or inconsistent sizes (K in {64, 128, 192, 256}; B*T < 2^31)";
         case GDR_ERR_CHUNK: return "chunk_size must be 64";
-        case GDR_ERR_DTYPE: return "out_dtype must be GDR_F32 or GDR_BF16";
+        case GDR_ERR_DTYPE: return "unsupported dtype (k: bf16 or fp16; beta: fp32, bf16 or fp16; out: fp32, bf16 or fp16)";
         case GDR_ERR_ALIGN: return "pointer misaligned (k and out 16 B, g 4 B, beta 2 B, cu_seqlens 4 B)";
         case GDR_ERR_DEVICE: return "no usable CUDA device (an sm_103 GPU is required)";
         case GDR_ERR_CUDA: return "a CUDA runtime or driver call failed";
@@ -1099,21 +1162,25 @@ const char *gdr_status_string(int status) {
     }
 }
 
-int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t *cu_seqlens,
-                  int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size, int out_dtype,
-                  void *out, void *stream) {
+int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *beta, int beta_dtype,
+                     const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K,
+                     int chunk_size, int out_dtype, void *out, void *stream) {
     using namespace gdr;
     if (chunk_size != kChunk) return GDR_ERR_CHUNK;
-    if (out_dtype != GDR_F32 && out_dtype != GDR_BF16) return GDR_ERR_DTYPE;
-    if (B < 0 || T < 0 || H < 0 || K != kHeadK) return GDR_ERR_SHAPE;
+    if (k_dtype != GDR_BF16 && k_dtype != GDR_F16) return GDR_ERR_DTYPE;
+    if (beta && beta_dtype != GDR_F32 && beta_dtype != GDR_BF16 && beta_dtype != GDR_F16)
+        return GDR_ERR_DTYPE;
+    if (out_dtype != GDR_F32 && out_dtype != GDR_BF16 && out_dtype != GDR_F16) return GDR_ERR_DTYPE;
+    if (B < 0 || T < 0 || H < 0 || K < 64 || K > kMaxHeadK || K % 64 != 0) return GDR_ERR_SHAPE;
     if (B == 0 || T == 0 || H == 0) return GDR_OK;
     if (!k || !out) return GDR_ERR_NULL;
     const int64_t ntok = cu_seqlens ? T : B * T;
     if (B > (int64_t(1) << 31) || T > (int64_t(1) << 31) || ntok >= (int64_t(1) << 31) ||
         H > (int64_t(1) << 24) || (cu_seqlens == nullptr && B > ((int64_t(1) << 31) / T)))
         return GDR_ERR_SHAPE;
+    const uintptr_t beta_align = (beta && beta_dtype == GDR_F32) ? 3 : 1;
     if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
-        (reinterpret_cast<uintptr_t>(g) & 3) || (reinterpret_cast<uintptr_t>(beta) & 1) ||
+        (reinterpret_cast<uintptr_t>(g) & 3) || (reinterpret_cast<uintptr_t>(beta) & beta_align) ||
         (reinterpret_cast<uintptr_t>(cu_seqlens) & 3))
         return GDR_ERR_ALIGN;
 
@@ -1130,20 +1197,22 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
                                    static_cast<cuuint64_t>(H * K * 2)};
     const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kChunk)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (encode(&tmap, k_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+               3, const_cast<void *>(k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GDR_ERR_CUDA;
 
     CUtensorMap tmap_o;
     {
-        const int esz = out_dtype == GDR_BF16 ? 2 : 4;
+        const int esz = out_dtype == GDR_F32 ? 4 : 2;
+        const CUtensorMapDataType odt = out_dtype == GDR_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                        : out_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const cuuint64_t odims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(ntok)};
         const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(64 * esz), static_cast<cuuint64_t>(H * 64 * esz)};
         const cuuint32_t obox[3] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(kChunk)};
-        if (encode(&tmap_o, out_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                   3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        if (encode(&tmap_o, odt, 3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return GDR_ERR_CUDA;
@@ -1151,7 +1220,9 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
 
     Params prm;
     prm.g = g;
-    prm.beta = static_cast<const __nv_bfloat16 *>(beta);
+    prm.beta = beta;
+    prm.beta_kind = beta ? beta_dtype : GDR_F32;
+    prm.idesc = idesc_f16_kind(k_dtype == GDR_BF16);
     prm.cu = cu_seqlens;
     prm.out = out;
     prm.B = B;
@@ -1176,12 +1247,17 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t
     prm.wg_ds = static_cast<uint32_t>((2 * grid * kNumWG) / H);
     prm.wg_dh = static_cast<uint32_t>((2 * grid * kNumWG) % H);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (out_dtype == GDR_BF16)
-        kkt_solve_kernel<true><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
-    else
-        kkt_solve_kernel<false><<<static_cast<unsigned>(grid), kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
+    const unsigned gx = static_cast<unsigned>(grid);
+    kernel_for(out_dtype, static_cast<int>(K / 64))<<<gx, kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
+}
+
+int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t *cu_seqlens,
+                  int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size, int out_dtype,
+                  void *out, void *stream) {
+    return gdr_kkt_solve_ex(k, GDR_BF16, g, beta, GDR_BF16, cu_seqlens, B, T, H, K, chunk_size,
+                            out_dtype, out, stream);
 }
 
 int gdr_kkt_solve_device_status(int *status) {

@@ -37,9 +37,9 @@ extern "C" {
 typedef enum {
     GDR_OK = 0,
     GDR_ERR_NULL = -1,    /* a required pointer is NULL                        */
-    GDR_ERR_SHAPE = -2,   /* negative size, unsupported K, or size overflow    */
+    GDR_ERR_SHAPE = -2,   /* negative size, K not in {64,128,192,256}, overflow */
     GDR_ERR_CHUNK = -3,   /* chunk_size != 64                                  */
-    GDR_ERR_DTYPE = -4,   /* out_dtype is not a gdr_dtype value                */
+    GDR_ERR_DTYPE = -4,   /* a dtype argument outside the supported set        */
     GDR_ERR_ALIGN = -5,   /* a pointer is not aligned as documented below      */
     GDR_ERR_DEVICE = -6,  /* no current CUDA device, or it is not sm_103       */
     GDR_ERR_CUDA = -7,    /* a CUDA runtime/driver call failed (launch, TMA map) */
@@ -47,15 +47,16 @@ typedef enum {
 } gdr_status;
 
 typedef enum {
-    GDR_F32 = 0,          /* IEEE fp32 output                                 */
-    GDR_BF16 = 1          /* bfloat16 output, round-to-nearest-even from fp32 */
+    GDR_F32 = 0,          /* IEEE fp32                                         */
+    GDR_BF16 = 1,         /* bfloat16 (outputs: round-to-nearest-even from fp32) */
+    GDR_F16 = 2           /* IEEE fp16 (outputs: round-to-nearest-even from fp32) */
 } gdr_dtype;
 
 /*
  * gdr_kkt_solve - (I + A)^{-1} of every 64-token chunk and head.
  *
  *   k          bf16 [B, T, H, K] contiguous; with cu_seqlens: [1, T, H, K].
- *              16-byte aligned.  K must be 128.
+ *              16-byte aligned.  K is 64, 128, 192 or 256.
  *   g          fp32 [B, T, H] (same leading layout as k) chunk-local cumulative
  *              log-gate, or NULL (gate factor 1).  4-byte aligned.
  *   beta       bf16 [B, T, H], or NULL (beta = 1).  2-byte aligned.
@@ -69,7 +70,7 @@ typedef enum {
  *              enqueues nothing).  B*T must be below 2^31.
  *   chunk_size must be 64 (GDR_ERR_CHUNK otherwise, like the page's API, which
  *              raises ValueError for other chunk sizes).
- *   out_dtype  GDR_F32 or GDR_BF16.
+ *   out_dtype  GDR_F32, GDR_BF16 or GDR_F16.
  *   out        [B, T, H, 64] of out_dtype, 16-byte aligned.  Every row of a
  *              real token is fully written (zeros included); no separate
  *              zero-fill is needed.  Must not overlap the inputs.
@@ -80,6 +81,26 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta,
                   const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
                   int64_t K, int chunk_size, int out_dtype, void *out,
                   void *stream);
+
+/*
+ * gdr_kkt_solve_ex - the same operation for the other input types the page's
+ * unit tests cover (same page, "How was this patch tested": fp32, bf16 and fp16
+ * inputs; its API block takes k, g and beta of the caller's dtype).
+ *
+ *   k_dtype    GDR_BF16 or GDR_F16 (the Gram runs on the tensor cores in that
+ *              type; products are exact in the fp32 accumulator).  fp32 keys
+ *              return GDR_ERR_DTYPE.
+ *   beta_dtype GDR_F32 (4-byte aligned), GDR_BF16 or GDR_F16 (2-byte aligned);
+ *              ignored when beta is NULL.
+ *   out_dtype  GDR_F32, GDR_BF16 or GDR_F16.
+ * Every other argument, the alignment rules, the return codes and the
+ * ownership and stream conventions are those of gdr_kkt_solve, which equals
+ * gdr_kkt_solve_ex(k, GDR_BF16, g, beta, GDR_BF16, ...).
+ */
+int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *beta,
+                     int beta_dtype, const int32_t *cu_seqlens, int64_t B, int64_t T,
+                     int64_t H, int64_t K, int chunk_size, int out_dtype, void *out,
+                     void *stream);
 
 /* Human-readable text for a gdr_status value (static storage, never NULL). */
 const char *gdr_status_string(int status);

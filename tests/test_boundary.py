@@ -58,12 +58,49 @@ def test_chunk_size_must_be_64(chunk):
     assert _call(chunk=chunk) == gdr.GDR_ERR_CHUNK
 
 
-@pytest.mark.parametrize("dtype", [-1, 2, 7])
+@pytest.mark.parametrize("dtype", [-1, 3, 7])
 def test_bad_out_dtype(dtype):
     assert _call(dtype=dtype) == gdr.GDR_ERR_DTYPE
 
 
-@pytest.mark.parametrize("kw", [dict(K=64), dict(K=256), dict(K=127), dict(B=-1), dict(T=-5),
+def _call_ex(**kw):
+    a = dict(k=K_PTR, kd=gdr.GDR_BF16, g=G_PTR, beta=B_PTR, bd=gdr.GDR_BF16, cu=0, B=2, T=100, H=3,
+             K=128, chunk=64, dtype=gdr.GDR_F32, out=OUT_PTR)
+    a.update(kw)
+    return gdr.kkt_solve_ex_raw(a["k"], a["kd"], a["g"], a["beta"], a["bd"], a["cu"], a["B"], a["T"],
+                                a["H"], a["K"], a["chunk"], a["dtype"], a["out"], 0)
+
+
+@pytest.mark.parametrize("kw", [dict(kd=gdr.GDR_F32), dict(kd=3), dict(kd=-1), dict(bd=3),
+                                dict(bd=-1), dict(dtype=3)])
+def test_ex_bad_dtypes(kw):
+    assert _call_ex(**kw) == gdr.GDR_ERR_DTYPE
+
+
+def test_ex_beta_dtype_ignored_without_beta():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this test covers the no-device path")
+    assert _call_ex(beta=0, bd=99) == gdr.GDR_ERR_DEVICE
+
+
+@pytest.mark.parametrize("kw", [dict(beta=B_PTR + 2, bd=gdr.GDR_F32), dict(beta=B_PTR + 1, bd=gdr.GDR_F16),
+                                dict(k=K_PTR + 8, kd=gdr.GDR_F16)])
+def test_ex_misaligned(kw):
+    assert _call_ex(**kw) == gdr.GDR_ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw", [dict(K=64), dict(K=192), dict(K=256), dict(kd=gdr.GDR_F16),
+                                dict(bd=gdr.GDR_F32), dict(bd=gdr.GDR_F16), dict(dtype=gdr.GDR_F16),
+                                dict(beta=B_PTR + 2, bd=gdr.GDR_F16)])
+def test_ex_valid_arguments_reach_the_device_check(kw):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this test covers the no-device path")
+    assert _call_ex(**kw) == gdr.GDR_ERR_DEVICE
+
+
+@pytest.mark.parametrize("kw", [dict(K=0), dict(K=32), dict(K=127), dict(K=320), dict(B=-1), dict(T=-5),
                                 dict(H=-2), dict(B=1 << 20, T=1 << 12),
                                 dict(cu=CU_PTR, B=4, T=1 << 31)])
 def test_bad_shapes(kw):

@@ -8,8 +8,9 @@ Recipe (the published workloads are not available, these stand in for them;
 the shapes are the ones quoted on the MindSpeed-Ops PR page "feat(triton): add
 chunk_gated_delta_rule_fwd_kkt_solve", performance table):
   * k    ~ N(0, 1) in fp32, L2-normalised over the head dimension K for every
-           (token, head), then rounded to bf16 (round-to-nearest-even).
-  * beta = sigmoid(N(0, 1)), rounded to bf16.
+           (token, head), then rounded to bf16 (round-to-nearest-even), or to
+           fp16 for the fp16-input variants.
+  * beta = sigmoid(N(0, 1)), rounded to bf16 (or fp16, or kept fp32).
   * g    = per-token U(-0.1, 0) log-decay in fp32, summed inclusively inside
            every 64-token chunk; the sum restarts at each chunk start, and
            chunks restart at every sequence start.
@@ -42,6 +43,8 @@ class Workload:
     varlen_lengths: Optional[tuple] = None   # per-sequence lengths when packed
     use_g: bool = True
     use_beta: bool = True
+    k_dtype: str = "bf16"       # "bf16" or "f16": type k is rounded to
+    beta_dtype: str = "bf16"    # "bf16", "f16" or "f32"
 
     @property
     def token_heads(self) -> int:
@@ -101,8 +104,8 @@ def _chunk_local_cumsum(a: np.ndarray, bounds) -> np.ndarray:
 
 
 def make_inputs(wl: Workload):
-    """Returns a dict of CPU tensors: k (bf16), g (fp32 or None), beta (bf16 or
-    None), cu_seqlens (int32 or None).  Fixed-length k is [B, T, H, K]; packed
+    """Returns a dict of CPU tensors: k (bf16 or fp16), g (fp32 or None), beta
+    (bf16, fp16, fp32 or None), cu_seqlens (int32 or None).  Fixed-length k is [B, T, H, K]; packed
     (varlen) k is [1, T, H, K]."""
     rng = np.random.default_rng(wl.seed)
     ntok = wl.B * wl.T if wl.varlen_lengths is None else wl.T
@@ -119,11 +122,12 @@ def make_inputs(wl: Workload):
     g = _chunk_local_cumsum(a.astype(np.float32), _sequence_bounds(wl))
 
     lead = (wl.B, wl.T) if wl.varlen_lengths is None else (1, wl.T)
-    kt = torch.from_numpy(k).to(torch.bfloat16).reshape(*lead, H, K)
+    types = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+    kt = torch.from_numpy(k).to(types[wl.k_dtype]).reshape(*lead, H, K)
     out = {
         "k": kt,
         "g": torch.from_numpy(g).reshape(*lead, H) if wl.use_g else None,
-        "beta": torch.from_numpy(beta.astype(np.float32)).to(torch.bfloat16).reshape(*lead, H)
+        "beta": torch.from_numpy(beta.astype(np.float32)).to(types[wl.beta_dtype]).reshape(*lead, H)
         if wl.use_beta else None,
         "cu_seqlens": None,
     }
