@@ -38,13 +38,16 @@ UNIT = "token-heads/s"
 PAGE_FUSED_MS = {"c5": 4.9368}
 
 
+ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4}
+
+
 def bytes_per_token_head(wl, out_dtype: str) -> int:
-    """Algorithmic HBM bytes per token-head: read k (K bf16), g (fp32), beta
-    (bf16); write one output row of 64 values."""
-    b = wl.K * 2
+    """Algorithmic HBM bytes per token-head: read k (K values), g (fp32), beta;
+    write one output row of 64 values."""
+    b = wl.K * ELEM_BYTES[wl.k_dtype]
     b += 4 if wl.use_g else 0
-    b += 2 if wl.use_beta else 0
-    b += 64 * (2 if out_dtype == "bf16" else 4)
+    b += ELEM_BYTES[wl.beta_dtype] if wl.use_beta else 0
+    b += 64 * ELEM_BYTES[out_dtype]
     return b
 
 
@@ -227,7 +230,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c5", choices=sorted(workloads.CONFIGS))
-    ap.add_argument("--out-dtype", default=None, choices=["f32", "bf16"])
+    ap.add_argument("--out-dtype", default=None, choices=["f32", "bf16", "f16"])
+    ap.add_argument("--K", type=int, default=None, choices=[64, 128, 192, 256],
+                    help="head dimension (default: the workload's, 128)")
+    ap.add_argument("--k-dtype", default="bf16", choices=["bf16", "f16"])
+    ap.add_argument("--beta-dtype", default="bf16", choices=["bf16", "f16", "f32"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -237,6 +244,11 @@ def main():
         ap.error("--warmup must be >= 3")
 
     wl = workloads.CONFIGS[args.config]
+    if args.K is not None and args.K != wl.K:
+        wl = wl.with_(K=args.K, name=wl.name.replace(f"_K{wl.K}", f"_K{args.K}"))
+    if args.k_dtype != wl.k_dtype or args.beta_dtype != wl.beta_dtype:
+        wl = wl.with_(k_dtype=args.k_dtype, beta_dtype=args.beta_dtype,
+                      name=f"{wl.name}_k{args.k_dtype}_beta{args.beta_dtype}")
     out_dtype = args.out_dtype or wl.out_dtype
     if args.impl == "reference":
         return run_reference(args, wl)
@@ -256,20 +268,20 @@ def main():
     g = None if inp["g"] is None else inp["g"].to(dev)
     beta = None if inp["beta"] is None else inp["beta"].to(dev)
     cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].to(dev)
-    odt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    odt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[out_dtype]
+    codes = {"bf16": gdr.GDR_BF16, "f16": gdr.GDR_F16, "f32": gdr.GDR_F32}
     out = torch.empty((*k.shape[:3], 64), dtype=odt, device=dev)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
     B = cu.numel() - 1 if cu is not None else k.shape[0]
 
     def step(o=out):
-        rc = gdr.kkt_solve_raw(k.data_ptr(), 0 if g is None else g.data_ptr(),
-                               0 if beta is None else beta.data_ptr(),
-                               0 if cu is None else cu.data_ptr(), B, k.shape[1], wl.H, wl.K, 64,
-                               gdr.GDR_BF16 if out_dtype == "bf16" else gdr.GDR_F32,
-                               o.data_ptr(), sh)
+        rc = gdr.kkt_solve_ex_raw(k.data_ptr(), codes[wl.k_dtype], 0 if g is None else g.data_ptr(),
+                                  0 if beta is None else beta.data_ptr(), codes[wl.beta_dtype],
+                                  0 if cu is None else cu.data_ptr(), B, k.shape[1], wl.H, wl.K, 64,
+                                  codes[out_dtype], o.data_ptr(), sh)
         if rc != gdr.GDR_OK:
-            raise gdr.GdrError(rc, "gdr_kkt_solve")
+            raise gdr.GdrError(rc, "gdr_kkt_solve_ex")
 
     def barrier():
         if ws > 1:
@@ -346,11 +358,12 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": (value / (th_rank / (PAGE_FUSED_MS[args.config] * 1e-3))
-                            if args.config in PAGE_FUSED_MS else None),
+                            if args.config in PAGE_FUSED_MS and wl.K == 128 else None),
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "K": wl.K,
-                       "chunk": 64, "k": "bf16", "g": "f32", "beta": "bf16", "out": out_dtype,
-                       "compute": "Gram bf16xbf16->f32 (tcgen05), gate/solve f32",
+                       "chunk": 64, "k": wl.k_dtype, "g": "f32", "beta": wl.beta_dtype,
+                       "out": out_dtype,
+                       "compute": f"Gram {wl.k_dtype}x{wl.k_dtype}->f32 (tcgen05), gate/solve f32",
                        "l2": f"no flush: inputs+output {th_rank * bpt / 1e6:.0f} MB/step > 129 MB L2",
                        "parallelism": f"replicas x{ws} (independent tiles, no collective)",
                        "vs_baseline_ref": "Ascend 910B fused Triton time from the PR page table"},
