@@ -47,6 +47,14 @@ def _load():
             lib.oracle_kkt_solve_chunk.restype = ctypes.c_int
             lib.oracle_kkt_solve.argtypes = [d, d, d, vp, i64, i64, i64, i64, i64, d, i64, i64]
             lib.oracle_kkt_solve.restype = ctypes.c_int
+            lib.oracle_chunk_A_chunk.argtypes = [i64, i64, i64, d, i64, d, i64, d, i64, d, i64]
+            lib.oracle_chunk_A_chunk.restype = ctypes.c_int
+            lib.oracle_solve_tril_chunk.argtypes = [i64, i64, d, i64, d, i64]
+            lib.oracle_solve_tril_chunk.restype = ctypes.c_int
+            lib.oracle_chunk_A.argtypes = [d, d, d, vp, i64, i64, i64, i64, i64, d, i64, i64]
+            lib.oracle_chunk_A.restype = ctypes.c_int
+            lib.oracle_solve_tril.argtypes = [d, vp, i64, i64, i64, i64, d, i64, i64]
+            lib.oracle_solve_tril.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -147,3 +155,59 @@ def kkt_solve_ref_chunk(kc, gc=None, bc=None, chunk_size: int = 64) -> np.ndarra
     if rc:
         raise RuntimeError("oracle chunk failed")
     return o
+
+
+def _layout(lead, cu_seqlens):
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int32))
+        return cu, len(cu) - 1, lead[1]
+    return None, lead[0], lead[1]
+
+
+def _over_heads(H, threads, run):
+    threads = max(1, min(threads or os.cpu_count() or 1, H))
+    bounds = [(H * t // threads, H * (t + 1) // threads) for t in range(threads)]
+    if threads == 1:
+        rcs = [run(0, H)]
+    else:
+        with _cf.ThreadPoolExecutor(threads) as ex:
+            rcs = list(ex.map(lambda b: run(*b), bounds))
+    if any(rcs):
+        raise RuntimeError(f"oracle failed: {rcs}")
+
+
+def chunk_A_ref(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64,
+                threads: int | None = None) -> np.ndarray:
+    """A of every chunk and head in float64, in the page's layout [B, T, H, chunk]:
+    A[i][j] = beta_i (k_i . k_j) exp(g_i - g_j) for j < i, zero elsewhere; rows
+    outside every sequence are 0."""
+    lib = _load()
+    kd = _f64(k)
+    lead = kd.shape[:2]
+    H, K = kd.shape[2], kd.shape[3]
+    ntok = lead[0] * lead[1]
+    kd = kd.reshape(ntok, H, K)
+    gd = None if g is None else _f64(g).reshape(ntok, H)
+    bd = None if beta is None else _f64(beta).reshape(ntok, H)
+    A = np.zeros((ntok, H, chunk_size), dtype=np.float64)
+    cu, nseq, T = _layout(lead, cu_seqlens)
+    _over_heads(H, threads, lambda hb, he: lib.oracle_chunk_A(
+        _ptr(kd), _ptr(gd), _ptr(bd), _ptr(cu), nseq, T, H, K, chunk_size, _ptr(A), hb, he))
+    return A.reshape(*lead, H, chunk_size)
+
+
+def solve_tril_ref(A, cu_seqlens=None, chunk_size: int = 64, threads: int | None = None) -> np.ndarray:
+    """(I + A)^{-1} of every chunk and head from a given A [B, T, H, chunk]
+    (only its strictly lower part inside each chunk is read), in float64."""
+    lib = _load()
+    Ad = _f64(A)
+    lead = Ad.shape[:2]
+    H = Ad.shape[2]
+    ntok = lead[0] * lead[1]
+    Ad = np.ascontiguousarray(Ad.reshape(ntok, H, chunk_size))
+    out = np.zeros((ntok, H, chunk_size), dtype=np.float64)
+    cu, nseq, T = _layout(lead, cu_seqlens)
+    _over_heads(H, threads, lambda hb, he: lib.oracle_solve_tril(
+        _ptr(Ad), _ptr(cu), nseq, T, H, chunk_size, _ptr(out), hb, he))
+    return out.reshape(*lead, H, chunk_size)

@@ -25,6 +25,14 @@
  *     are allowed.
  *   - PyPTO page "GatedDeltaRule算子性能优化案例", section 3.3.1: the inverse is
  *     a fixed-count row-by-row update, which is the forward substitution above.
+ * The two halves of that chain are also given on their own, as the page's
+ * unfused chain has them (same page, "What this PR does": the fused call
+ * replaces chunk_scaled_dot_kkt_fwd followed by solve_tril, which write and
+ * read A as [B, T, H, chunk]):
+ *   oracle_chunk_A*      A itself, rows of real tokens, zero on and above the
+ *                        diagonal and past the chunk;
+ *   oracle_solve_tril*   (I + A)^{-1} of a given A by the same substitution,
+ *                        reading only its strictly lower part.
  * Readings where the pages are silent: beta scales row i; the exponent is not
  *   clamped here (the Ascend kernel clamps it to [-50, 50], which never binds
  *   for chunk-local decays); g = NULL means g = 0, beta = NULL means beta = 1.
@@ -112,6 +120,105 @@ int oracle_kkt_solve(const double *k, const double *g, const double *beta,
                     g ? g + c0 * H + h : NULL, H,
                     beta ? beta + c0 * H + h : NULL, H,
                     out + (c0 * H + h) * C, H * C);
+                if (rc)
+                    return rc;
+            }
+        }
+    }
+    return 0;
+}
+
+/* A of one chunk: out row r is A[r][0..C), A[i][j] as above for j < i < L and
+ * 0 elsewhere.  Same arguments as oracle_kkt_solve_chunk. */
+int oracle_chunk_A_chunk(int64_t L, int64_t C, int64_t K,
+                         const double *kc, int64_t ldk,
+                         const double *g, int64_t ldg,
+                         const double *beta, int64_t ldb,
+                         double *out, int64_t ldo)
+{
+    for (int64_t i = 0; i < L; ++i) {
+        for (int64_t j = 0; j < C; ++j) {
+            double a = 0.0;
+            if (j < i) {
+                double dot = 0.0;
+                for (int64_t d = 0; d < K; ++d)
+                    dot += kc[i * ldk + d] * kc[j * ldk + d];
+                double bi = beta ? beta[i * ldb] : 1.0;
+                double gate = g ? exp(g[i * ldg] - g[j * ldg]) : 1.0;
+                a = bi * dot * gate;
+            }
+            out[i * ldo + j] = a;
+        }
+    }
+    return 0;
+}
+
+/* (I + A)^{-1} of one chunk from a given A (row r is Ain[r*lda + j]; only
+ * j < r < L is read), by forward substitution; out rows as in
+ * oracle_kkt_solve_chunk.  Returns 0, or -1 when a scratch allocation fails. */
+int oracle_solve_tril_chunk(int64_t L, int64_t C, const double *Ain, int64_t lda,
+                            double *out, int64_t ldo)
+{
+    double *X = (double *)calloc((size_t)(L * L), sizeof(double));
+    if (!X)
+        return -1;
+    for (int64_t i = 0; i < L; ++i) {
+        for (int64_t c = 0; c < L; ++c) {
+            double v = (i == c) ? 1.0 : 0.0;
+            for (int64_t j = 0; j < i; ++j)
+                v -= Ain[i * lda + j] * X[j * L + c];
+            X[i * L + c] = v;
+        }
+    }
+    for (int64_t i = 0; i < L; ++i)
+        for (int64_t c = 0; c < C; ++c)
+            out[i * ldo + c] = (c < L) ? X[i * L + c] : 0.0;
+    free(X);
+    return 0;
+}
+
+/* Whole-tensor forms for heads [h_begin, h_end), with the sequence layout of
+ * oracle_kkt_solve.  oracle_chunk_A writes A [Ntok, H, C] from k, g, beta;
+ * oracle_solve_tril reads A [Ntok, H, C] and writes out [Ntok, H, C]. */
+int oracle_chunk_A(const double *k, const double *g, const double *beta,
+                   const int32_t *cu, int64_t nseq, int64_t T, int64_t H,
+                   int64_t K, int64_t C, double *A,
+                   int64_t h_begin, int64_t h_end)
+{
+    if (!k || !A || nseq < 0 || T < 0 || H <= 0 || K <= 0 || C <= 0)
+        return -2;
+    for (int64_t n = 0; n < nseq; ++n) {
+        int64_t s = cu ? (int64_t)cu[n] : n * T;
+        int64_t e = cu ? (int64_t)cu[n + 1] : (n + 1) * T;
+        if (e < s)
+            return -2;
+        for (int64_t c0 = s; c0 < e; c0 += C) {
+            int64_t L = (e - c0 < C) ? (e - c0) : C;
+            for (int64_t h = h_begin; h < h_end; ++h)
+                oracle_chunk_A_chunk(L, C, K, k + (c0 * H + h) * K, H * K,
+                                     g ? g + c0 * H + h : NULL, H,
+                                     beta ? beta + c0 * H + h : NULL, H,
+                                     A + (c0 * H + h) * C, H * C);
+        }
+    }
+    return 0;
+}
+
+int oracle_solve_tril(const double *A, const int32_t *cu, int64_t nseq, int64_t T,
+                      int64_t H, int64_t C, double *out, int64_t h_begin, int64_t h_end)
+{
+    if (!A || !out || nseq < 0 || T < 0 || H <= 0 || C <= 0)
+        return -2;
+    for (int64_t n = 0; n < nseq; ++n) {
+        int64_t s = cu ? (int64_t)cu[n] : n * T;
+        int64_t e = cu ? (int64_t)cu[n + 1] : (n + 1) * T;
+        if (e < s)
+            return -2;
+        for (int64_t c0 = s; c0 < e; c0 += C) {
+            int64_t L = (e - c0 < C) ? (e - c0) : C;
+            for (int64_t h = h_begin; h < h_end; ++h) {
+                int rc = oracle_solve_tril_chunk(L, C, A + (c0 * H + h) * C, H * C,
+                                                 out + (c0 * H + h) * C, H * C);
                 if (rc)
                     return rc;
             }

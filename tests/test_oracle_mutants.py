@@ -2,7 +2,9 @@
 that the pins catch every one of them.  This is evidence that the pins in
 test_oracle_pins.py constrain each part of the definition: the beta index, the
 gate sign and base, the dot product, the sign of A, the orientation of the
-result, the substitution's operand order, the diagonal and the chunk restart."""
+result, the substitution's operand order, the diagonal and the chunk restart,
+and in the unfused chain's halves the gate, the strictness of A and the
+solve's operand order and sign."""
 import ctypes
 import os
 import subprocess
@@ -27,6 +29,12 @@ MUTANTS = {
     "no_unit_diagonal": ("double v = (i == c) ? 1.0 : 0.0;", "double v = 0.0;"),
     "global_chunk_grid": ("for (int64_t c0 = s; c0 < e; c0 += C) {",
                           "for (int64_t c0 = s - (s % C); c0 < e; c0 += C) {"),
+    # the halves of the unfused chain
+    "A_gate_divides": ("a = bi * dot * gate;", "a = bi * dot / gate;"),
+    "A_keeps_diagonal": ("if (j < i) {", "if (j <= i) {"),
+    "solve_reads_transposed_A": ("v -= Ain[i * lda + j] * X[j * L + c];",
+                                 "v -= Ain[j * lda + i] * X[j * L + c];"),
+    "solve_i_minus_a": ("v -= Ain[i * lda + j] * X[j * L + c];", "v += Ain[i * lda + j] * X[j * L + c];"),
 }
 
 # Pins to run against each mutant (function, kwargs).
@@ -38,6 +46,10 @@ PINS = [
     (pins.test_collinear_keys_delta_rule_product_form, {}),
     (pins.test_varlen_equals_separate_sequences, {}),
     (pins.test_golden_fixture_reproduces, {}),
+    (pins.test_chunk_A_hand_values, {}),
+    (pins.test_solve_tril_equals_library_inverse_and_reads_only_strict_lower, {}),
+    (pins.test_solve_tril_L3_closed_form, {}),
+    (pins.test_chain_of_halves_equals_fused_oracle, dict(name="c1")),
 ]
 
 
@@ -51,7 +63,8 @@ def _build_mutant(tmp_path, name, old, new):
     subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", str(so), str(c), "-lm"])
     lib = ctypes.CDLL(str(so))
     real = oracle._load()
-    for fn in ("oracle_kkt_solve_chunk", "oracle_kkt_solve"):
+    for fn in ("oracle_kkt_solve_chunk", "oracle_kkt_solve", "oracle_chunk_A_chunk",
+               "oracle_solve_tril_chunk", "oracle_chunk_A", "oracle_solve_tril"):
         getattr(lib, fn).argtypes = getattr(real, fn).argtypes
         getattr(lib, fn).restype = getattr(real, fn).restype
     return lib

@@ -288,3 +288,66 @@ def test_golden_fixture_reproduces():
             assert np.max(np.abs(out[r, h] - vals)) <= 1e-12
             n += 1
     assert n > 0
+
+
+# ---------------------------------------------------------------------------
+# The two halves of the unfused chain (A alone, and the solve of a given A).
+
+def test_chunk_A_hand_values():
+    # L = 3, K = 2, C = 4.  Keys, beta and g chosen so that beta_i vs beta_j,
+    # the gate sign and exp vs exp2 all give different numbers.
+    k = np.array([[1.0, 0.0], [0.5, 0.5], [2.0, 1.0]])
+    beta = np.array([0.3, 0.5, 0.25])
+    g = np.array([0.0, -math.log(2.0), -math.log(4.0)])
+    A = oracle.chunk_A_ref(k.reshape(1, 3, 1, 2), g.reshape(1, 3, 1), beta.reshape(1, 3, 1),
+                           chunk_size=4)[0, :, 0, :]
+    want = np.zeros((3, 4))
+    want[1, 0] = 0.5 * 0.5 * 0.5          # beta_1 (k1.k0) e^{g1-g0}
+    want[2, 0] = 0.25 * 2.0 * 0.25        # beta_2 (k2.k0) e^{g2-g0}
+    want[2, 1] = 0.25 * 1.5 * 0.5         # beta_2 (k2.k1) e^{g2-g1}
+    assert np.array_equal(A, want)
+
+
+def test_solve_tril_equals_library_inverse_and_reads_only_strict_lower():
+    rng = np.random.default_rng(91)
+    L = 37
+    A = np.tril(rng.standard_normal((L, L)) * 0.2, k=-1)
+    noisy = A + np.triu(rng.standard_normal((L, L)))          # diagonal and upper: ignored
+    full = np.zeros((1, L, 1, C))
+    full[0, :, 0, :L] = noisy
+    full[0, :, 0, L:] = 7.0
+    X = oracle.solve_tril_ref(full, cu_seqlens=np.array([0, L], dtype=np.int32))[0, :, 0, :]
+    assert np.abs(X[:, :L] - np.linalg.inv(np.eye(L) + A)).max() <= 1e-12
+    assert np.all(X[:, L:] == 0.0)
+
+
+def test_solve_tril_L3_closed_form():
+    a10, a20, a21 = 0.7, -0.4, 1.3
+    A = np.zeros((1, 3, 1, C))
+    A[0, 1, 0, 0], A[0, 2, 0, 0], A[0, 2, 0, 1] = a10, a20, a21
+    X = oracle.solve_tril_ref(A, cu_seqlens=np.array([0, 3], dtype=np.int32))[0, :, 0, :3]
+    want = np.array([[1.0, 0.0, 0.0], [-a10, 1.0, 0.0], [a21 * a10 - a20, -a21, 1.0]])
+    assert np.abs(X - want).max() <= 1e-15
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "varlen"])
+def test_chain_of_halves_equals_fused_oracle(name):
+    if name == "varlen":
+        lens = (1, 64, 0, 65, 130, 2)
+        wl = workloads.Workload("chain_varlen", len(lens), sum(lens), 3, 32, "f32", seed=93,
+                                varlen_lengths=lens)
+    else:
+        wl = workloads.CONFIGS[name].with_(T=min(workloads.CONFIGS[name].T, 300))
+    inp = workloads.make_inputs(wl)
+    A = oracle.chunk_A_ref(inp["k"], inp["g"], inp["beta"], inp["cu_seqlens"])
+    X = oracle.solve_tril_ref(A, inp["cu_seqlens"])
+    ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], inp["cu_seqlens"])
+    assert np.abs(X - ref).max() <= 1e-12
+    # A is strictly lower inside each chunk and zero past the chunk's length.
+    Af = A.reshape(-1, wl.H, C)
+    for s, e in workloads._sequence_bounds(wl):
+        for c0 in range(s, e, C):
+            L = min(C, e - c0)
+            blk = Af[c0:c0 + L]                              # [L, H, C]
+            upper = np.arange(C)[None, :] >= np.arange(L)[:, None]
+            assert np.all(blk.transpose(0, 2, 1)[upper] == 0.0)
