@@ -31,8 +31,9 @@ GDR_F32 = 0
 GDR_BF16 = 1
 GDR_F16 = 2
 
-EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_kkt_solve_ex", "gdr_status_string",
-                    "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms")
+EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_kkt_solve_ex", "gdr_chunk_scaled_dot_kkt",
+                    "gdr_solve_tril", "gdr_status_string", "gdr_kkt_solve_device_status",
+                    "gdr_kkt_solve_num_sms")
 
 _lib = None
 _lock = threading.Lock()
@@ -66,6 +67,10 @@ def load_library():
             lib.gdr_kkt_solve.restype = ci
             lib.gdr_kkt_solve_ex.argtypes = [vp, ci, vp, vp, ci, vp, i64, i64, i64, i64, ci, ci, vp, vp]
             lib.gdr_kkt_solve_ex.restype = ci
+            lib.gdr_chunk_scaled_dot_kkt.argtypes = [vp, ci, vp, vp, ci, vp, i64, i64, i64, i64, ci, vp, vp]
+            lib.gdr_chunk_scaled_dot_kkt.restype = ci
+            lib.gdr_solve_tril.argtypes = [vp, vp, i64, i64, i64, ci, ci, vp, vp]
+            lib.gdr_solve_tril.restype = ci
             lib.gdr_status_string.argtypes = [ci]
             lib.gdr_status_string.restype = ctypes.c_char_p
             lib.gdr_kkt_solve_device_status.argtypes = [ctypes.POINTER(ci)]
@@ -95,6 +100,23 @@ def kkt_solve_ex_raw(k_ptr: int, k_dtype: int, g_ptr: int, beta_ptr: int, beta_d
     return load_library().gdr_kkt_solve_ex(k_ptr or None, k_dtype, g_ptr or None, beta_ptr or None,
                                            beta_dtype, cu_ptr or None, B, T, H, K, chunk_size,
                                            out_dtype, out_ptr or None, stream or None)
+
+
+def chunk_scaled_dot_kkt_raw(k_ptr: int, k_dtype: int, g_ptr: int, beta_ptr: int, beta_dtype: int,
+                             cu_ptr: int, B: int, T: int, H: int, K: int, chunk_size: int,
+                             A_ptr: int, stream: int) -> int:
+    """Direct call of gdr_chunk_scaled_dot_kkt with integer pointers; returns the status."""
+    return load_library().gdr_chunk_scaled_dot_kkt(k_ptr or None, k_dtype, g_ptr or None,
+                                                   beta_ptr or None, beta_dtype, cu_ptr or None,
+                                                   B, T, H, K, chunk_size, A_ptr or None,
+                                                   stream or None)
+
+
+def solve_tril_raw(A_ptr: int, cu_ptr: int, B: int, T: int, H: int, chunk_size: int,
+                   out_dtype: int, out_ptr: int, stream: int) -> int:
+    """Direct call of gdr_solve_tril with integer pointers; returns the status."""
+    return load_library().gdr_solve_tril(A_ptr or None, cu_ptr or None, B, T, H, chunk_size,
+                                         out_dtype, out_ptr or None, stream or None)
 
 
 def _gdr_dtype(dt, what: str) -> int:
@@ -177,5 +199,88 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
     return out
 
 
-__all__ = ["kkt_solve", "kkt_solve_raw", "kkt_solve_ex_raw", "device_status", "num_sms", "build", "load_library",
+def _check_inputs(k, g, beta, cu_seqlens, chunk_size):
+    import torch
+
+    if chunk_size != 64:
+        raise ValueError("chunk_size must be 64")
+    if k.dtype not in (torch.bfloat16, torch.float16) or k.dim() != 4 or not k.is_cuda:
+        raise TypeError("k must be a 4-D bf16 or fp16 CUDA tensor")
+    for name, t, dt in (("g", g, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)):
+        if t is not None and (t.dtype != dt or t.device != k.device):
+            raise TypeError(f"{name} must be a {dt} tensor on {k.device}")
+    if beta is not None and beta.device != k.device:
+        raise TypeError(f"beta must be on {k.device}")
+    Bk, T, H, _ = k.shape
+    for name, t in (("g", g), ("beta", beta)):
+        if t is not None and tuple(t.shape) != (Bk, T, H):
+            raise ValueError(f"{name} must have shape {(Bk, T, H)}")
+    if cu_seqlens is not None and (Bk != 1 or cu_seqlens.dim() != 1):
+        raise ValueError("with cu_seqlens, k must be [1, T, H, K] and cu_seqlens 1-D")
+    return cu_seqlens.numel() - 1 if cu_seqlens is not None else Bk
+
+
+def chunk_scaled_dot_kkt(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, A=None,
+                         stream=None):
+    """The unfused chain's first half: A [B, T, H, 64] fp32 with
+    A[i][j] = beta_i (k_i . k_j) exp(g_i - g_j) for j < i, zero elsewhere."""
+    import torch
+
+    B = _check_inputs(k, g, beta, cu_seqlens, chunk_size)
+    Bk, T, H, K = k.shape
+    k = k.contiguous()
+    g = None if g is None else g.contiguous()
+    beta = None if beta is None else beta.contiguous()
+    if A is None:
+        A = torch.empty((Bk, T, H, 64), dtype=torch.float32, device=k.device)
+    elif A.dtype != torch.float32 or tuple(A.shape) != (Bk, T, H, 64) or not A.is_contiguous():
+        raise ValueError("A has the wrong dtype, shape or layout")
+    if stream is None:
+        stream = torch.cuda.current_stream(k.device).cuda_stream
+    with torch.cuda.device(k.device):
+        rc = chunk_scaled_dot_kkt_raw(k.data_ptr(), _gdr_dtype(k.dtype, "k"),
+                                      0 if g is None else g.data_ptr(),
+                                      0 if beta is None else beta.data_ptr(),
+                                      GDR_F32 if beta is None else _gdr_dtype(beta.dtype, "beta"),
+                                      0 if cu_seqlens is None else cu_seqlens.contiguous().data_ptr(),
+                                      B, T, H, K, chunk_size, A.data_ptr(), int(stream))
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_chunk_scaled_dot_kkt")
+    return A
+
+
+def solve_tril(A, cu_seqlens=None, chunk_size: int = 64, output_dtype=None, out=None, stream=None):
+    """The unfused chain's second half: (I + A)^{-1} of every chunk from A
+    [B, T, H, 64] fp32 (only each chunk's strictly lower part is read)."""
+    import torch
+
+    if chunk_size != 64:
+        raise ValueError("chunk_size must be 64")
+    if A.dtype != torch.float32 or A.dim() != 4 or A.shape[3] != 64 or not A.is_cuda:
+        raise TypeError("A must be a [B, T, H, 64] fp32 CUDA tensor")
+    if output_dtype is None:
+        output_dtype = torch.float32
+    out_code = _gdr_dtype(output_dtype, "output_dtype")
+    Bk, T, H, _ = A.shape
+    if cu_seqlens is not None:
+        if Bk != 1 or cu_seqlens.dim() != 1 or cu_seqlens.dtype != torch.int32:
+            raise ValueError("with cu_seqlens, A must be [1, T, H, 64] and cu_seqlens 1-D int32")
+        B = cu_seqlens.numel() - 1
+    else:
+        B = Bk
+    A = A.contiguous()
+    if out is None:
+        out = torch.empty((Bk, T, H, 64), dtype=output_dtype, device=A.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    with torch.cuda.device(A.device):
+        rc = solve_tril_raw(A.data_ptr(), 0 if cu_seqlens is None else cu_seqlens.contiguous().data_ptr(),
+                            B, T, H, chunk_size, out_code, out.data_ptr(), int(stream))
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_solve_tril")
+    return out
+
+
+__all__ = ["kkt_solve", "chunk_scaled_dot_kkt", "solve_tril", "kkt_solve_raw", "kkt_solve_ex_raw",
+           "chunk_scaled_dot_kkt_raw", "solve_tril_raw", "device_status", "num_sms", "build", "load_library",
            "status_string", "GdrError", "EXPORTED_SYMBOLS"]

@@ -684,14 +684,27 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
     return out != 0;
 }
 
+// Modes: the fused step; its first half alone (A = beta K K^T exp(gate), strictly
+// lower, written to HBM as fp32 like the page's chunk_scaled_dot_kkt_fwd); its
+// second half alone ((I + A)^{-1} from that A, like the page's solve_tril).  The
+// halves run the fused step's own code, so the two-kernel chain reproduces the
+// fused result bit for bit.
+constexpr int kModeFused = 0, kModeKkt = 1, kModeSolve = 2;
+
 // OUT: kOutF32, kOutBF16 or kOutF16.  The merge runs split (fp32-accurate) for
 // fp32 and fp16 output and as one tf32 pass for bf16 output.  NKB = K / 64, the
 // 64-column key boxes per row; it only shapes the producer and MMA loops, which
-// sit on the pipeline's critical path and so are fully unrolled per K.
-template <int OUT, int NKB>
+// sit on the pipeline's critical path and so are fully unrolled per K.  In the
+// solve mode the producer loads A tiles (two 32-column fp32 boxes per tile,
+// NKB = 2) and the MMA warp has nothing to do.
+template <int OUT, int NKB, int MODE>
 __global__ void __launch_bounds__(kNumThreads, 1)
     kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_out, const Params p) {
+    static_assert(MODE != kModeKkt || OUT == kOutF32, "A is written as fp32");
+    static_assert(MODE != kModeSolve || NKB == 2, "an A tile row is two 128-byte boxes");
+    constexpr bool kUseTmem = MODE != kModeSolve;
+    constexpr int kBoxCols = MODE == kModeSolve ? 32 : 64;   // elements per 128-byte box row
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -710,7 +723,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNumStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            // Freed by the MMA commit, or in the solve mode by the 4 warps of the
+            // warpgroup that copied the stage.
+            mbar_init(bar_empty + 8 * s, kUseTmem ? 1 : 4);
         }
         for (int w = 0; w < kNumWG; ++w) {
             mbar_init(bar_tfull + 8 * w, 1);
@@ -719,14 +734,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kMmaWarp) {
+    if (kUseTmem && warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = kUseTmem ? *tmem_slot : 0u;
 
     const int64_t n_local = (p.n_pairs > blockIdx.x)
                                 ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
@@ -763,7 +778,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         if (t.L > 0)
 #pragma unroll
                             for (int kb = 0; kb < nkb; ++kb)
-                                tma_prefetch_3d(&tmap_k, 64 * kb, t.h, static_cast<int>(t.row0));
+                                tma_prefetch_3d(&tmap_k, kBoxCols * kb, t.h, static_cast<int>(t.row0));
                         walk_advance(p, w, p.pair_ds, p.pair_dh);
                     }
                 } else if (q + 1 < n_local) {
@@ -791,7 +806,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                         for (int kh = 0; kh < nb; ++kh)
                             tma_load_3d(st + (2 * kh + tt) * kBoxBytes, &tmap_k, bar_full + 8 * s,
-                                        64 * (2 * kc + kh), t.h, static_cast<int>(t.row0));
+                                        kBoxCols * (2 * kc + kh), t.h, static_cast<int>(t.row0));
                 }
                 if (failed) break;
             }
@@ -808,7 +823,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+        if (kUseTmem && lane == 0) {
             int64_t q = 0;          // ends as the number of pairs whose Gram was committed
             bool failed = false;
             for (; q < n_local; ++q) {
@@ -890,8 +905,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const RowIn rnext = load_row(p, nx, i_e);
 
             if ((qd & 1) == 0 && lane == 0) bulk_wait_read();   // this warp's previous store
+            // The warpgroup's input: its Gram in TMEM, or in the solve mode its A
+            // tiles in stage wg (pair q = wg + 3r uses stage q % 3 = wg).
+            const uint32_t bar_in = kUseTmem ? bar_tfull + 8 * wg : bar_full + 8 * wg;
             if (qd == 3 && lane == 0) {
-                int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
+                int ok = mbar_wait(bar_in, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
                 wg_flag[wg] = ok;
             }
@@ -904,7 +922,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const bool rowok = i_e < te.L;
             float ui = 1.0f, vi = 1.0f;
             bool unsafe = false;
-            if (p.g && rowok) {
+            if (MODE != kModeSolve && p.g && rowok) {
                 const float d = rin.g - 0.5f * (rin.gfirst + rin.glast);
                 unsafe = !(fabsf(d) <= 30.0f);
                 ui = expf(d);
@@ -916,9 +934,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             vcur[i_e] = rowok ? vi : 0.0f;
             const bool direct = named_bar_red_or(bar_id, 128, unsafe);   // B2: g, v ready; A free
             if (!wg_flag[wg]) break;
-            tc_fence_after();
+            if constexpr (kUseTmem) tc_fence_after();
 
-            // ---- epilogue: S row from TMEM -> A row in shared memory
+            // ---- epilogue: S row from TMEM -> A row in shared memory (in the kkt
+            //      mode: into the fp32 staging, masked to the strict lower part);
+            //      solve mode: A row from the stage -> shared memory
+            if constexpr (MODE == kModeSolve) {
+                // Every thread acquires the stage's completed phase itself.
+                if (!mbar_wait(bar_in, static_cast<uint32_t>(r & 1))) record_timeout(p, abort_flag);
+                const uint8_t *sa = smem + kOffK + wg * kStageBytes + tt_e * kBoxBytes + i_e * 128;
+                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + i_e * kAPitch);
+                const int n4 = (qd & 1) ? 16 : 8;
+#pragma unroll
+                for (int j4 = 0; j4 < 16; ++j4) {
+                    if (j4 < n4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(
+                            sa + (j4 >> 3) * 2 * kBoxBytes + (((j4 & 7) ^ (i_e & 7)) << 4));
+                        Arow[j4] = rowok ? v : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * wg);
+            } else
             {
                 uint32_t sr[64];
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
@@ -937,13 +974,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
 
                 float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + i_e * kAPitch);
-                // Rows 0..31 only need columns j < 32 (A is strictly lower).
-                const int n4 = (qd & 1) ? 16 : 8;
+                // Rows 0..31 only need columns j < 32 (A is strictly lower).  The
+                // kkt mode writes whole rows, zero at and above the diagonal.
+                const int n4 = (MODE == kModeKkt || (qd & 1)) ? 16 : 8;
+                uint8_t *const sk = abuf + (tt_e ? kStage1Off : 0);
+                auto put = [&](int j4, float4 a) {
+                    if constexpr (MODE == kModeKkt) {
+                        const int j = 4 * j4;
+                        a.x = j + 0 < i_e ? a.x : 0.0f;
+                        a.y = j + 1 < i_e ? a.y : 0.0f;
+                        a.z = j + 2 < i_e ? a.z : 0.0f;
+                        a.w = j + 3 < i_e ? a.w : 0.0f;
+                        *reinterpret_cast<float4 *>(sk + stage_piece_off<false>(i_e, j4)) = a;
+                    } else {
+                        Arow[j4] = a;
+                    }
+                };
                 if (!rowok) {
                     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int j4 = 0; j4 < 16; ++j4)
-                        if (j4 < n4) Arow[j4] = z;
+                        if (j4 < n4) put(j4, z);
                 } else if (!direct) {
                     const float w = beta_value(p, rin.beta) * ui;
 #pragma unroll
@@ -955,7 +1006,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             a.y = (__uint_as_float(sr[4 * j4 + 1]) * w) * v.y;
                             a.z = (__uint_as_float(sr[4 * j4 + 2]) * w) * v.z;
                             a.w = (__uint_as_float(sr[4 * j4 + 3]) * w) * v.w;
-                            Arow[j4] = a;
+                            put(j4, a);
                         }
                     }
                 } else {
@@ -973,55 +1024,58 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                   __expf(fminf(fmaxf(gi - gj.z, -50.f), 50.f));
                             a.w = bi * __uint_as_float(sr[4 * j4 + 3]) *
                                   __expf(fminf(fmaxf(gi - gj.w, -50.f), 50.f));
-                            Arow[j4] = a;
+                            put(j4, a);
                         }
                     }
                 }
             }
-            // The diagonal blocks this warp inverts below are exactly the 32 rows it
-            // has just written (tile qd >> 1, rows 32 (qd & 1) ..), so a warp-level
-            // barrier is enough here.
-            __syncwarp();
+            // The kkt mode is done: its rows are in the staging.
+            if constexpr (MODE != kModeKkt) {
+                // The diagonal blocks this warp inverts below are exactly the 32 rows it
+                // has just written (tile qd >> 1, rows 32 (qd & 1) ..), so a warp-level
+                // barrier is enough here.
+                __syncwarp();
 
-            // ---- diagonal inverses: thread -> (tile, block I, row c)
-            const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
-            float drow[16];
-            diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
-            {
-                float4 *dst = reinterpret_cast<float4 *>(At(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
-                                                         16 * dslot_c(dI));
-#pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4)
-                    dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
-            }
-            named_bar_sync(bar_id, 128);                       // B3b: D blocks ready
+                // ---- diagonal inverses: thread -> (tile, block I, row c)
+                const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
+                float drow[16];
+                diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
+                {
+                    float4 *dst = reinterpret_cast<float4 *>(At(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
+                                                             16 * dslot_c(dI));
+    #pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
+                }
+                named_bar_sync(bar_id, 128);                       // B3b: D blocks ready
 
-            // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column);
-            //      then X rows are assembled in the A buffer (after B4 in both branches)
-            const int mt = qd & 1;
-            uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
-            if (qd < 2) {
-                float z0[3][2][4];
-                merge_column<0, OUT != kOutBF16>(At(mt), g8, t4, z0);
-                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                stage_block_T<OUT>(st_m, 1, 0, z0[0], g8, t4);
-                stage_block_T<OUT>(st_m, 2, 0, z0[1], g8, t4);
-                stage_block_T<OUT>(st_m, 3, 0, z0[2], g8, t4);
-            } else {
-                float z1[2][2][4], z2[1][2][4];
-                merge_column<1, OUT != kOutBF16>(At(mt), g8, t4, z1);
-                merge_column<2, OUT != kOutBF16>(At(mt), g8, t4, z2);
-                named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
-                stage_block_T<OUT>(st_m, 2, 1, z1[0], g8, t4);
-                stage_block_T<OUT>(st_m, 3, 1, z1[1], g8, t4);
-                stage_block_T<OUT>(st_m, 3, 2, z2[0], g8, t4);
-            }
-            {
-                const float4 dv[4] = {make_float4(drow[0], drow[1], drow[2], drow[3]),
-                                      make_float4(drow[4], drow[5], drow[6], drow[7]),
-                                      make_float4(drow[8], drow[9], drow[10], drow[11]),
-                                      make_float4(drow[12], drow[13], drow[14], drow[15])};
-                stage_diag_row<OUT>(abuf + (dt ? kStage1Off : 0), 16 * dI + dc, dI, dv);
+                // ---- off-diagonal blocks on tensor cores: warp -> (tile, block column);
+                //      then X rows are assembled in the A buffer (after B4 in both branches)
+                const int mt = qd & 1;
+                uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
+                if (qd < 2) {
+                    float z0[3][2][4];
+                    merge_column<0, OUT != kOutBF16>(At(mt), g8, t4, z0);
+                    named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
+                    stage_block_T<OUT>(st_m, 1, 0, z0[0], g8, t4);
+                    stage_block_T<OUT>(st_m, 2, 0, z0[1], g8, t4);
+                    stage_block_T<OUT>(st_m, 3, 0, z0[2], g8, t4);
+                } else {
+                    float z1[2][2][4], z2[1][2][4];
+                    merge_column<1, OUT != kOutBF16>(At(mt), g8, t4, z1);
+                    merge_column<2, OUT != kOutBF16>(At(mt), g8, t4, z2);
+                    named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
+                    stage_block_T<OUT>(st_m, 2, 1, z1[0], g8, t4);
+                    stage_block_T<OUT>(st_m, 3, 1, z1[1], g8, t4);
+                    stage_block_T<OUT>(st_m, 3, 2, z2[0], g8, t4);
+                }
+                {
+                    const float4 dv[4] = {make_float4(drow[0], drow[1], drow[2], drow[3]),
+                                          make_float4(drow[4], drow[5], drow[6], drow[7]),
+                                          make_float4(drow[8], drow[9], drow[10], drow[11]),
+                                          make_float4(drow[12], drow[13], drow[14], drow[15])};
+                    stage_diag_row<OUT>(abuf + (dt ? kStage1Off : 0), 16 * dI + dc, dI, dv);
+                }
             }
             fence_proxy_async_smem();
             named_bar_sync(bar_id, 128);                       // B5: X complete
@@ -1062,7 +1116,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (kUseTmem && warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
@@ -1085,21 +1139,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 using KernelFn = void (*)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap, Params);
 
-template <int OUT>
+template <int OUT, int MODE>
 KernelFn kernel_for_nkb(int nkb) {
     switch (nkb) {
-        case 1: return kkt_solve_kernel<OUT, 1>;
-        case 2: return kkt_solve_kernel<OUT, 2>;
-        case 3: return kkt_solve_kernel<OUT, 3>;
-        default: return kkt_solve_kernel<OUT, 4>;
+        case 1: return kkt_solve_kernel<OUT, 1, MODE>;
+        case 2: return kkt_solve_kernel<OUT, 2, MODE>;
+        case 3: return kkt_solve_kernel<OUT, 3, MODE>;
+        default: return kkt_solve_kernel<OUT, 4, MODE>;
     }
 }
 
-// The instantiation for an output kind (gdr_dtype value) and K / 64.
-KernelFn kernel_for(int out_kind, int nkb) {
-    if (out_kind == kOutBF16) return kernel_for_nkb<kOutBF16>(nkb);
-    if (out_kind == kOutF16) return kernel_for_nkb<kOutF16>(nkb);
-    return kernel_for_nkb<kOutF32>(nkb);
+// The instantiation for a mode, an output kind (gdr_dtype value) and K / 64.
+KernelFn kernel_for(int mode, int out_kind, int nkb) {
+    if (mode == kModeKkt) return kernel_for_nkb<kOutF32, kModeKkt>(nkb);
+    if (mode == kModeSolve) {
+        if (out_kind == kOutBF16) return kkt_solve_kernel<kOutBF16, 2, kModeSolve>;
+        if (out_kind == kOutF16) return kkt_solve_kernel<kOutF16, 2, kModeSolve>;
+        return kkt_solve_kernel<kOutF32, 2, kModeSolve>;
+    }
+    if (out_kind == kOutBF16) return kernel_for_nkb<kOutBF16, kModeFused>(nkb);
+    if (out_kind == kOutF16) return kernel_for_nkb<kOutF16, kModeFused>(nkb);
+    return kernel_for_nkb<kOutF32, kModeFused>(nkb);
 }
 
 constexpr int kMaxDevices = 64;
@@ -1126,10 +1186,12 @@ int prepare_device(int *sms) {
             return GDR_ERR_DEVICE;
         }
         bool attr_ok = true;
-        for (int o = 0; o < 3; ++o)
-            for (int n = 1; n <= 4; ++n)
-                attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(o, n), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                          kSmemBytes) == cudaSuccess;
+        for (int m = 0; m < 3; ++m)
+            for (int o = 0; o < 3; ++o)
+                for (int n = 1; n <= 4; ++n)
+                    attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(m, o, n),
+                                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                              kSmemBytes) == cudaSuccess;
         if (!attr_ok) {
             cudaGetLastError();
             return GDR_ERR_CUDA;
@@ -1162,24 +1224,31 @@ const char *gdr_status_string(int status) {
     }
 }
 
-int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *beta, int beta_dtype,
-                     const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K,
-                     int chunk_size, int out_dtype, void *out, void *stream) {
-    using namespace gdr;
+}  // extern "C"
+
+namespace gdr {
+
+// Validates the arguments and enqueues one launch of the given mode.  `in` is
+// the key tensor (fused and kkt modes; in_dtype bf16 or fp16, K columns) or the
+// fp32 A tensor (solve mode; 64 columns).  The kkt mode writes fp32 A to `out`.
+int launch(int mode, const void *in, int in_dtype, const float *g, const void *beta, int beta_dtype,
+           const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size,
+           int out_dtype, void *out, void *stream) {
     if (chunk_size != kChunk) return GDR_ERR_CHUNK;
-    if (k_dtype != GDR_BF16 && k_dtype != GDR_F16) return GDR_ERR_DTYPE;
+    if (mode == kModeSolve ? in_dtype != GDR_F32 : (in_dtype != GDR_BF16 && in_dtype != GDR_F16))
+        return GDR_ERR_DTYPE;
     if (beta && beta_dtype != GDR_F32 && beta_dtype != GDR_BF16 && beta_dtype != GDR_F16)
         return GDR_ERR_DTYPE;
     if (out_dtype != GDR_F32 && out_dtype != GDR_BF16 && out_dtype != GDR_F16) return GDR_ERR_DTYPE;
     if (B < 0 || T < 0 || H < 0 || K < 64 || K > kMaxHeadK || K % 64 != 0) return GDR_ERR_SHAPE;
     if (B == 0 || T == 0 || H == 0) return GDR_OK;
-    if (!k || !out) return GDR_ERR_NULL;
+    if (!in || !out) return GDR_ERR_NULL;
     const int64_t ntok = cu_seqlens ? T : B * T;
     if (B > (int64_t(1) << 31) || T > (int64_t(1) << 31) || ntok >= (int64_t(1) << 31) ||
         H > (int64_t(1) << 24) || (cu_seqlens == nullptr && B > ((int64_t(1) << 31) / T)))
         return GDR_ERR_SHAPE;
     const uintptr_t beta_align = (beta && beta_dtype == GDR_F32) ? 3 : 1;
-    if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
+    if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
         (reinterpret_cast<uintptr_t>(g) & 3) || (reinterpret_cast<uintptr_t>(beta) & beta_align) ||
         (reinterpret_cast<uintptr_t>(cu_seqlens) & 3))
         return GDR_ERR_ALIGN;
@@ -1190,28 +1259,37 @@ int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *bet
     auto encode = encode_fn();
     if (!encode) return GDR_ERR_CUDA;
 
+    // Input tiles: 64 rows x 128 bytes per box (64 bf16/fp16 key columns, or 32
+    // fp32 columns of A), 128-byte swizzle.
     CUtensorMap tmap;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(H),
-                                static_cast<cuuint64_t>(ntok)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K * 2),
-                                   static_cast<cuuint64_t>(H * K * 2)};
-    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kChunk)};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&tmap, k_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-               3, const_cast<void *>(k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return GDR_ERR_CUDA;
-
+    {
+        const int esz = mode == kModeSolve ? 4 : 2;
+        const int64_t cols = mode == kModeSolve ? 64 : K;
+        const CUtensorMapDataType dt = mode == kModeSolve   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : in_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(H),
+                                    static_cast<cuuint64_t>(ntok)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * esz),
+                                       static_cast<cuuint64_t>(H * cols * esz)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(kChunk)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&tmap, dt, 3, const_cast<void *>(in), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GDR_ERR_CUDA;
+    }
+    const int out_kind = mode == kModeKkt ? GDR_F32 : out_dtype;
     CUtensorMap tmap_o;
     {
-        const int esz = out_dtype == GDR_F32 ? 4 : 2;
-        const CUtensorMapDataType odt = out_dtype == GDR_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                        : out_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const int esz = out_kind == GDR_F32 ? 4 : 2;
+        const CUtensorMapDataType odt = out_kind == GDR_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                        : out_kind == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const cuuint64_t odims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(ntok)};
         const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(64 * esz), static_cast<cuuint64_t>(H * 64 * esz)};
         const cuuint32_t obox[3] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(kChunk)};
+        const cuuint32_t estr[3] = {1, 1, 1};
         if (encode(&tmap_o, odt, 3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -1219,10 +1297,10 @@ int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *bet
     }
 
     Params prm;
-    prm.g = g;
-    prm.beta = beta;
-    prm.beta_kind = beta ? beta_dtype : GDR_F32;
-    prm.idesc = idesc_f16_kind(k_dtype == GDR_BF16);
+    prm.g = mode == kModeSolve ? nullptr : g;
+    prm.beta = mode == kModeSolve ? nullptr : beta;
+    prm.beta_kind = prm.beta ? beta_dtype : GDR_F32;
+    prm.idesc = idesc_f16_kind(in_dtype == GDR_BF16);
     prm.cu = cu_seqlens;
     prm.out = out;
     prm.B = B;
@@ -1248,9 +1326,33 @@ int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *bet
     prm.wg_dh = static_cast<uint32_t>((2 * grid * kNumWG) % H);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned gx = static_cast<unsigned>(grid);
-    kernel_for(out_dtype, static_cast<int>(K / 64))<<<gx, kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
+    kernel_for(mode, out_kind, static_cast<int>(K / 64))<<<gx, kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
+}
+
+}  // namespace gdr
+
+extern "C" {
+
+int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *beta, int beta_dtype,
+                     const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K,
+                     int chunk_size, int out_dtype, void *out, void *stream) {
+    return gdr::launch(gdr::kModeFused, k, k_dtype, g, beta, beta_dtype, cu_seqlens, B, T, H, K,
+                       chunk_size, out_dtype, out, stream);
+}
+
+int gdr_chunk_scaled_dot_kkt(const void *k, int k_dtype, const float *g, const void *beta,
+                             int beta_dtype, const int32_t *cu_seqlens, int64_t B, int64_t T,
+                             int64_t H, int64_t K, int chunk_size, float *A, void *stream) {
+    return gdr::launch(gdr::kModeKkt, k, k_dtype, g, beta, beta_dtype, cu_seqlens, B, T, H, K,
+                       chunk_size, GDR_F32, A, stream);
+}
+
+int gdr_solve_tril(const float *A, const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
+                   int chunk_size, int out_dtype, void *out, void *stream) {
+    return gdr::launch(gdr::kModeSolve, A, GDR_F32, nullptr, nullptr, GDR_F32, cu_seqlens, B, T, H,
+                       64, chunk_size, out_dtype, out, stream);
 }
 
 int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t *cu_seqlens,

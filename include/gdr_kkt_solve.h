@@ -102,6 +102,33 @@ int gdr_kkt_solve_ex(const void *k, int k_dtype, const float *g, const void *bet
                      int64_t H, int64_t K, int chunk_size, int out_dtype, void *out,
                      void *stream);
 
+/*
+ * The unfused chain, in two calls, as on the same page ("What this PR does":
+ * the fused call replaces chunk_scaled_dot_kkt_fwd followed by solve_tril, with
+ * A passed between them through HBM as [B, T, H, 64]).  It is the baseline
+ * that measures the fusion: A makes a round trip through HBM (256 bytes per
+ * token-head written and read again).  Both calls run the fused kernel's own
+ * arithmetic, so gdr_solve_tril(gdr_chunk_scaled_dot_kkt(...)) equals
+ * gdr_kkt_solve_ex(...) bit for bit.
+ *
+ * gdr_chunk_scaled_dot_kkt - writes A [B, T, H, 64] fp32 (16-byte aligned):
+ *   A[i][j] = beta_i (k_i . k_j) exp(g_i - g_j) for j < i < L, and exactly 0 on
+ *   and above the diagonal and in columns >= L.  Rows of tokens outside every
+ *   sequence are not written.  Other arguments as in gdr_kkt_solve_ex.
+ */
+int gdr_chunk_scaled_dot_kkt(const void *k, int k_dtype, const float *g, const void *beta,
+                             int beta_dtype, const int32_t *cu_seqlens, int64_t B, int64_t T,
+                             int64_t H, int64_t K, int chunk_size, float *A, void *stream);
+
+/*
+ * gdr_solve_tril - out = (I + A)^{-1} of every chunk and head from A [B, T, H,
+ *   64] fp32 (16-byte aligned; only the strictly lower part of each chunk's
+ *   L x L block is read).  cu_seqlens, B, T, H, chunk_size, out_dtype and out
+ *   as in gdr_kkt_solve.
+ */
+int gdr_solve_tril(const float *A, const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
+                   int chunk_size, int out_dtype, void *out, void *stream);
+
 /* Human-readable text for a gdr_status value (static storage, never NULL). */
 const char *gdr_status_string(int status);
 

@@ -147,3 +147,38 @@ def test_product_path_does_not_import_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "oracle_kkt_solve" not in text, fn
+
+
+def _call_kkt(**kw):
+    a = dict(k=K_PTR, kd=gdr.GDR_BF16, g=G_PTR, beta=B_PTR, bd=gdr.GDR_BF16, cu=0, B=2, T=100, H=3,
+             K=128, chunk=64, A=OUT_PTR)
+    a.update(kw)
+    return gdr.chunk_scaled_dot_kkt_raw(a["k"], a["kd"], a["g"], a["beta"], a["bd"], a["cu"], a["B"],
+                                        a["T"], a["H"], a["K"], a["chunk"], a["A"], 0)
+
+
+def _call_solve(**kw):
+    a = dict(A=K_PTR, cu=0, B=2, T=100, H=3, chunk=64, dtype=gdr.GDR_F32, out=OUT_PTR)
+    a.update(kw)
+    return gdr.solve_tril_raw(a["A"], a["cu"], a["B"], a["T"], a["H"], a["chunk"], a["dtype"],
+                              a["out"], 0)
+
+
+@pytest.mark.parametrize("call,kw,want", [
+    (_call_kkt, dict(chunk=32), gdr.GDR_ERR_CHUNK), (_call_kkt, dict(A=0), gdr.GDR_ERR_NULL),
+    (_call_kkt, dict(A=OUT_PTR + 4), gdr.GDR_ERR_ALIGN), (_call_kkt, dict(kd=gdr.GDR_F32), gdr.GDR_ERR_DTYPE),
+    (_call_kkt, dict(K=96), gdr.GDR_ERR_SHAPE), (_call_kkt, dict(B=0), gdr.GDR_OK),
+    (_call_solve, dict(chunk=128), gdr.GDR_ERR_CHUNK), (_call_solve, dict(A=0), gdr.GDR_ERR_NULL),
+    (_call_solve, dict(out=0), gdr.GDR_ERR_NULL), (_call_solve, dict(A=K_PTR + 8), gdr.GDR_ERR_ALIGN),
+    (_call_solve, dict(dtype=5), gdr.GDR_ERR_DTYPE), (_call_solve, dict(T=-1), gdr.GDR_ERR_SHAPE),
+    (_call_solve, dict(H=0), gdr.GDR_OK)])
+def test_unfused_chain_argument_checks(call, kw, want):
+    assert call(**kw) == want
+
+
+def test_unfused_chain_valid_arguments_reach_the_device_check():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this test covers the no-device path")
+    assert _call_kkt() == gdr.GDR_ERR_DEVICE
+    assert _call_solve() == gdr.GDR_ERR_DEVICE
