@@ -316,6 +316,44 @@ def main():
     if gdr.device_status() != gdr.GDR_OK:
         raise RuntimeError("device status not ok after the timed region")
 
+    # The unfused chain on the same inputs (A through HBM, two launches), timed
+    # the same way: what the fusion saves on this GPU.
+    A = torch.empty((*k.shape[:3], 64), dtype=torch.float32, device=dev)
+
+    def kkt_half():
+        rc = gdr.chunk_scaled_dot_kkt_raw(k.data_ptr(), codes[wl.k_dtype], 0 if g is None else g.data_ptr(),
+                                          0 if beta is None else beta.data_ptr(), codes[wl.beta_dtype],
+                                          0 if cu is None else cu.data_ptr(), B, k.shape[1], wl.H, wl.K,
+                                          64, A.data_ptr(), sh)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_chunk_scaled_dot_kkt")
+
+    def solve_half():
+        rc = gdr.solve_tril_raw(A.data_ptr(), 0 if cu is None else cu.data_ptr(), B, k.shape[1], wl.H,
+                                64, codes[out_dtype], out.data_ptr(), sh)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_solve_tril")
+
+    chain_steps = max(10, min(args.steps, 2000))
+    chain_ms = {}
+    for name, fns in (("chain", (kkt_half, solve_half)), ("kkt", (kkt_half,)), ("solve", (solve_half,))):
+        for _ in range(3):
+            for f in fns:
+                f()
+        torch.cuda.synchronize(dev)
+        barrier()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(chain_steps):
+            for f in fns:
+                f()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        chain_ms[name] = reduce_max(c0.elapsed_time(c1) / chain_steps, ws, dev)
+    if gdr.device_status() != gdr.GDR_OK:
+        raise RuntimeError("device status not ok after the unfused chain")
+    del A
+
     # End to end through the public API with host buffers: H2D of the step's
     # inputs from pinned memory, the call, D2H of the full output.
     hk = inp["k"].pin_memory()
@@ -376,6 +414,14 @@ def main():
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,
             "clocks": clocks,
+            "unfused_chain": {
+                "what": "gdr_chunk_scaled_dot_kkt then gdr_solve_tril (A fp32 through HBM), same inputs",
+                "value": aggregate_value(th_rank, chain_ms["chain"], ws), "unit": UNIT,
+                "ms_per_step": chain_ms["chain"], "steps": chain_steps, "launches_per_step": 2,
+                "kkt_ms": chain_ms["kkt"], "solve_ms": chain_ms["solve"],
+                "bytes_per_token_head": bpt + 2 * 64 * 4,
+                "fused_speedup": chain_ms["chain"] / ms_step,
+            },
         }
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_budget)
