@@ -27,13 +27,14 @@ GDR_ERR_ALIGN = -5
 GDR_ERR_DEVICE = -6
 GDR_ERR_CUDA = -7
 GDR_ERR_TIMEOUT = -8
+GDR_ERR_SCRATCH = -9
 GDR_F32 = 0
 GDR_BF16 = 1
 GDR_F16 = 2
 
 EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_kkt_solve_ex", "gdr_chunk_scaled_dot_kkt",
-                    "gdr_solve_tril", "gdr_status_string", "gdr_kkt_solve_device_status",
-                    "gdr_kkt_solve_num_sms")
+                    "gdr_solve_tril", "gdr_kkt_solve_unfused_noalloc", "gdr_status_string",
+                    "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms")
 
 _lib = None
 _lock = threading.Lock()
@@ -71,6 +72,9 @@ def load_library():
             lib.gdr_chunk_scaled_dot_kkt.restype = ci
             lib.gdr_solve_tril.argtypes = [vp, vp, i64, i64, i64, ci, ci, vp, vp]
             lib.gdr_solve_tril.restype = ci
+            lib.gdr_kkt_solve_unfused_noalloc.argtypes = [vp, ci, vp, vp, ci, vp, i64, i64, i64, i64, ci, ci,
+                                                          vp, vp]
+            lib.gdr_kkt_solve_unfused_noalloc.restype = ci
             lib.gdr_status_string.argtypes = [ci]
             lib.gdr_status_string.restype = ctypes.c_char_p
             lib.gdr_kkt_solve_device_status.argtypes = [ctypes.POINTER(ci)]
@@ -117,6 +121,18 @@ def solve_tril_raw(A_ptr: int, cu_ptr: int, B: int, T: int, H: int, chunk_size: 
     """Direct call of gdr_solve_tril with integer pointers; returns the status."""
     return load_library().gdr_solve_tril(A_ptr or None, cu_ptr or None, B, T, H, chunk_size,
                                          out_dtype, out_ptr or None, stream or None)
+
+
+def kkt_solve_unfused_noalloc_raw(k_ptr: int, k_dtype: int, g_ptr: int, beta_ptr: int,
+                                  beta_dtype: int, cu_ptr: int, B: int, T: int, H: int, K: int,
+                                  chunk_size: int, out_dtype: int, out_ptr: int, stream: int) -> int:
+    """Direct call of gdr_kkt_solve_unfused_noalloc (the allocation-free chain, for
+    callers that may not allocate device memory while running; at most 262144
+    token-heads per call); returns the gdr_status code."""
+    return load_library().gdr_kkt_solve_unfused_noalloc(k_ptr or None, k_dtype, g_ptr or None,
+                                                        beta_ptr or None, beta_dtype, cu_ptr or None,
+                                                        B, T, H, K, chunk_size, out_dtype,
+                                                        out_ptr or None, stream or None)
 
 
 def _gdr_dtype(dt, what: str) -> int:
@@ -282,5 +298,5 @@ def solve_tril(A, cu_seqlens=None, chunk_size: int = 64, output_dtype=None, out=
 
 
 __all__ = ["kkt_solve", "chunk_scaled_dot_kkt", "solve_tril", "kkt_solve_raw", "kkt_solve_ex_raw",
-           "chunk_scaled_dot_kkt_raw", "solve_tril_raw", "device_status", "num_sms", "build", "load_library",
+           "chunk_scaled_dot_kkt_raw", "solve_tril_raw", "kkt_solve_unfused_noalloc_raw", "device_status", "num_sms", "build", "load_library",
            "status_string", "GdrError", "EXPORTED_SYMBOLS"]

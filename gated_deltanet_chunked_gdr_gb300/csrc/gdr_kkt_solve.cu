@@ -1166,6 +1166,38 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_ready[kMaxDevices];   // 0 unknown, 1 ready, -1 unsupported
 std::atomic<int> g_dev_sms[kMaxDevices];
 
+// Scratch of the allocation-free chain entry point: room for A of at most
+// kScratchTokenHeads token-heads (64 fp32 values each, 64 MiB in total).  It is
+// part of the library's device image, so every GPU that loads the library
+// holds it until the process exits.
+constexpr int64_t kScratchTokenHeads = int64_t(1) << 18;
+static __device__ __align__(256) float g_chain_scratch[kScratchTokenHeads * 64];
+
+// Device address of g_chain_scratch, looked up once per device with that device
+// current.  In host code the array's name stands for a host-side shadow, not
+// for device memory, so the address must come from cudaGetSymbolAddress.
+std::atomic<float *> g_scratch_addr[kMaxDevices];
+
+int scratch_for_current_device(float **addr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GDR_ERR_DEVICE;
+    }
+    float *a = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (a == nullptr) {
+        void *sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_chain_scratch) != cudaSuccess || sym == nullptr) {
+            cudaGetLastError();
+            return GDR_ERR_CUDA;
+        }
+        a = static_cast<float *>(sym);
+        g_scratch_addr[dev].store(a, std::memory_order_release);
+    }
+    *addr = a;
+    return GDR_OK;
+}
+
 int prepare_device(int *sms) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -1220,6 +1252,8 @@ const char *gdr_status_string(int status) {
         case GDR_ERR_DEVICE: return "no usable CUDA device (an sm_103 GPU is required)";
         case GDR_ERR_CUDA: return "a CUDA runtime or driver call failed";
         case GDR_ERR_TIMEOUT: return "a device-side pipeline wait timed out";
+        case GDR_ERR_SCRATCH:
+            return "problem too large for the allocation-free entry point (at most 262144 token-heads)";
         default: return "unknown gdr_status";
     }
 }
@@ -1231,9 +1265,11 @@ namespace gdr {
 // Validates the arguments and enqueues one launch of the given mode.  `in` is
 // the key tensor (fused and kkt modes; in_dtype bf16 or fp16, K columns) or the
 // fp32 A tensor (solve mode; 64 columns).  The kkt mode writes fp32 A to `out`.
-int launch(int mode, const void *in, int in_dtype, const float *g, const void *beta, int beta_dtype,
-           const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size,
-           int out_dtype, void *out, void *stream) {
+// Host-side argument checks of one launch; GDR_OK means a launch may follow
+// (or, for an empty problem, that nothing needs to run: see is_empty).
+int validate(int mode, const void *in, int in_dtype, const void *g, const void *beta, int beta_dtype,
+             const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size,
+             int out_dtype, const void *out) {
     if (chunk_size != kChunk) return GDR_ERR_CHUNK;
     if (mode == kModeSolve ? in_dtype != GDR_F32 : (in_dtype != GDR_BF16 && in_dtype != GDR_F16))
         return GDR_ERR_DTYPE;
@@ -1252,9 +1288,21 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
         (reinterpret_cast<uintptr_t>(g) & 3) || (reinterpret_cast<uintptr_t>(beta) & beta_align) ||
         (reinterpret_cast<uintptr_t>(cu_seqlens) & 3))
         return GDR_ERR_ALIGN;
+    return GDR_OK;
+}
+
+bool is_empty(int64_t B, int64_t T, int64_t H) { return B == 0 || T == 0 || H == 0; }
+
+int launch(int mode, const void *in, int in_dtype, const float *g, const void *beta, int beta_dtype,
+           const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size,
+           int out_dtype, void *out, void *stream) {
+    int rc = validate(mode, in, in_dtype, g, beta, beta_dtype, cu_seqlens, B, T, H, K, chunk_size,
+                      out_dtype, out);
+    if (rc != GDR_OK || is_empty(B, T, H)) return rc;
+    const int64_t ntok = cu_seqlens ? T : B * T;
 
     int sms = 0;
-    int rc = prepare_device(&sms);
+    rc = prepare_device(&sms);
     if (rc != GDR_OK) return rc;
     auto encode = encode_fn();
     if (!encode) return GDR_ERR_CUDA;
@@ -1353,6 +1401,31 @@ int gdr_solve_tril(const float *A, const int32_t *cu_seqlens, int64_t B, int64_t
                    int chunk_size, int out_dtype, void *out, void *stream) {
     return gdr::launch(gdr::kModeSolve, A, GDR_F32, nullptr, nullptr, GDR_F32, cu_seqlens, B, T, H,
                        64, chunk_size, out_dtype, out, stream);
+}
+
+int gdr_kkt_solve_unfused_noalloc(const void *k, int k_dtype, const float *g, const void *beta,
+                                  int beta_dtype, const int32_t *cu_seqlens, int64_t B, int64_t T,
+                                  int64_t H, int64_t K, int chunk_size, int out_dtype, void *out,
+                                  void *stream) {
+    using namespace gdr;
+    // The argument checks of both halves (with a stand-in, aligned scratch
+    // address), then the size limit; nothing is allocated anywhere on this path.
+    const float *const stand_in = reinterpret_cast<const float *>(uintptr_t(256));
+    int rc = validate(kModeKkt, k, k_dtype, g, beta, beta_dtype, cu_seqlens, B, T, H, K, chunk_size,
+                      GDR_F32, stand_in);
+    if (rc == GDR_OK)
+        rc = validate(kModeSolve, stand_in, GDR_F32, nullptr, nullptr, GDR_F32, cu_seqlens, B, T, H, 64,
+                      chunk_size, out_dtype, out);
+    if (rc != GDR_OK || is_empty(B, T, H)) return rc;
+    const int64_t ntok = cu_seqlens ? T : B * T;
+    if (ntok > kScratchTokenHeads || H > kScratchTokenHeads / ntok) return GDR_ERR_SCRATCH;
+    float *A = nullptr;
+    rc = scratch_for_current_device(&A);
+    if (rc != GDR_OK) return rc;
+    rc = gdr_chunk_scaled_dot_kkt(k, k_dtype, g, beta, beta_dtype, cu_seqlens, B, T, H, K, chunk_size,
+                                  A, stream);
+    if (rc != GDR_OK) return rc;
+    return gdr_solve_tril(A, cu_seqlens, B, T, H, chunk_size, out_dtype, out, stream);
 }
 
 int gdr_kkt_solve(const void *k, const float *g, const void *beta, const int32_t *cu_seqlens,

@@ -43,7 +43,8 @@ typedef enum {
     GDR_ERR_ALIGN = -5,   /* a pointer is not aligned as documented below      */
     GDR_ERR_DEVICE = -6,  /* no current CUDA device, or it is not sm_103       */
     GDR_ERR_CUDA = -7,    /* a CUDA runtime/driver call failed (launch, TMA map) */
-    GDR_ERR_TIMEOUT = -8  /* a device-side bounded wait ran out (see gdr_kkt_solve_device_status) */
+    GDR_ERR_TIMEOUT = -8, /* a device-side bounded wait ran out (see gdr_kkt_solve_device_status) */
+    GDR_ERR_SCRATCH = -9  /* too large for gdr_kkt_solve_unfused_noalloc's fixed scratch */
 } gdr_status;
 
 typedef enum {
@@ -128,6 +129,36 @@ int gdr_chunk_scaled_dot_kkt(const void *k, int k_dtype, const float *g, const v
  */
 int gdr_solve_tril(const float *A, const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
                    int chunk_size, int out_dtype, void *out, void *stream);
+
+/*
+ * gdr_kkt_solve_unfused_noalloc - the unfused chain above in one call that
+ * allocates nothing.  The paper has no counterpart; this entry point exists for
+ * callers that may not allocate device memory while they run: a serving
+ * runtime whose device memory is planned up front with a fixed budget, or code
+ * that cannot afford cudaMalloc's implicit device synchronisation.  They pass
+ * inputs and outputs as for gdr_kkt_solve_ex; A goes through a scratch array
+ * that is part of the library's device image (64 MiB on every GPU that loads
+ * the library, held until the process exits).
+ *
+ *   Limit: at most 262144 token-heads per call (B*T*H, or T*H with
+ *          cu_seqlens); larger problems return GDR_ERR_SCRATCH before anything
+ *          is enqueued.  Other arguments and checks are those of
+ *          gdr_kkt_solve_ex, and the result equals gdr_kkt_solve_ex's bit for
+ *          bit.
+ *   Set-up: the first call on a device, with that device current, looks up the
+ *          scratch's device address (cudaGetSymbolAddress) and keeps it for
+ *          later calls; make that first call before any stream capture.
+ *   Races:  every call on a device shares the one scratch array.  Calls whose
+ *          work overlaps on the GPU (different streams without ordering between
+ *          them, or several host threads on different streams) race on it and
+ *          give wrong results; order them, for example on one stream.  Nothing
+ *          in the scratch needs to start at zero: each call writes every row of
+ *          A that it later reads, and the array keeps the last call's contents.
+ */
+int gdr_kkt_solve_unfused_noalloc(const void *k, int k_dtype, const float *g, const void *beta,
+                                  int beta_dtype, const int32_t *cu_seqlens, int64_t B, int64_t T,
+                                  int64_t H, int64_t K, int chunk_size, int out_dtype, void *out,
+                                  void *stream);
 
 /* Human-readable text for a gdr_status value (static storage, never NULL). */
 const char *gdr_status_string(int status);

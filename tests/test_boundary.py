@@ -35,7 +35,7 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = gdr.status_string(code)
         assert isinstance(s, str) and s and s != "unknown gdr_status"
     assert gdr.status_string(-99) == "unknown gdr_status"
@@ -182,3 +182,29 @@ def test_unfused_chain_valid_arguments_reach_the_device_check():
         pytest.skip("a GPU is present; this test covers the no-device path")
     assert _call_kkt() == gdr.GDR_ERR_DEVICE
     assert _call_solve() == gdr.GDR_ERR_DEVICE
+
+
+def _call_noalloc(**kw):
+    a = dict(k=K_PTR, kd=gdr.GDR_BF16, g=G_PTR, beta=B_PTR, bd=gdr.GDR_BF16, cu=0, B=2, T=100, H=3,
+             K=128, chunk=64, dtype=gdr.GDR_F32, out=OUT_PTR)
+    a.update(kw)
+    return gdr.kkt_solve_unfused_noalloc_raw(a["k"], a["kd"], a["g"], a["beta"], a["bd"], a["cu"], a["B"],
+                                             a["T"], a["H"], a["K"], a["chunk"], a["dtype"], a["out"], 0)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(B=1, T=1 << 16, H=5), gdr.GDR_ERR_SCRATCH),          # 327680 token-heads > 262144
+    (dict(B=5, T=1 << 16, H=1), gdr.GDR_ERR_SCRATCH),
+    (dict(cu=CU_PTR, B=3, T=70000, H=4), gdr.GDR_ERR_SCRATCH),
+    (dict(chunk=32), gdr.GDR_ERR_CHUNK), (dict(out=0), gdr.GDR_ERR_NULL),
+    (dict(out=OUT_PTR + 8), gdr.GDR_ERR_ALIGN), (dict(dtype=9), gdr.GDR_ERR_DTYPE),
+    (dict(K=100), gdr.GDR_ERR_SHAPE), (dict(T=0), gdr.GDR_OK), (dict(H=-1), gdr.GDR_ERR_SHAPE)])
+def test_noalloc_argument_checks_and_size_limit(kw, want):
+    assert _call_noalloc(**kw) == want
+
+
+def test_noalloc_within_limit_reaches_the_device_check():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this test covers the no-device path")
+    assert _call_noalloc(B=1, T=1 << 16, H=4) == gdr.GDR_ERR_DEVICE     # exactly 262144
