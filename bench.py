@@ -47,7 +47,7 @@ def bytes_per_token_head(wl, out_dtype: str) -> int:
     b = wl.K * ELEM_BYTES[wl.k_dtype]
     b += 4 if wl.use_g else 0
     b += ELEM_BYTES[wl.beta_dtype] if wl.use_beta else 0
-    b += 64 * ELEM_BYTES[out_dtype]
+    b += wl.chunk * ELEM_BYTES[out_dtype]
     return b
 
 
@@ -173,19 +173,19 @@ def run_reference(args, wl):
     # Calibrate the per-tile cost, then size each step so K steps take <= ~60 s.
     calib = [tiles[i] for i in rng.choice(len(tiles), size=min(len(tiles), 4 * threads), replace=False)]
     t0 = time.perf_counter()
-    oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], calib, threads=threads)
+    oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], calib, chunk_size=wl.chunk, threads=threads)
     per_tile = (time.perf_counter() - t0) / len(calib)
     per_step = max(1, min(len(tiles), int(60.0 / max(1, args.steps) / per_tile)))
     samples = [[tiles[i] for i in rng.choice(len(tiles), size=per_step, replace=False)]
                for _ in range(min(args.steps, 8))]
     for w in range(args.warmup):
         oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], samples[w % len(samples)],
-                                   threads=threads)
+                                   chunk_size=wl.chunk, threads=threads)
     th = 0
     t0 = time.perf_counter()
     for s in range(args.steps):
         smp = samples[s % len(samples)]
-        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, threads=threads)
+        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, chunk_size=wl.chunk, threads=threads)
         th += sum(t[4] for t in smp)
     dt = time.perf_counter() - t0
     value = th / dt
@@ -215,7 +215,7 @@ def cpu_baseline(wl, inp, budget_s: float):
     batch = 8 * threads
     while done < len(tiles) and time.perf_counter() - t0 < budget_s:
         smp = [tiles[i] for i in order[done:done + batch]]
-        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, threads=threads)
+        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, chunk_size=wl.chunk, threads=threads)
         done += len(smp)
         th += sum(t[4] for t in smp)
     dt = time.perf_counter() - t0
@@ -234,6 +234,7 @@ def main():
     ap.add_argument("--K", type=int, default=None, choices=[64, 128, 192, 256],
                     help="head dimension (default: the workload's, 128)")
     ap.add_argument("--k-dtype", default="bf16", choices=["bf16", "f16"])
+    ap.add_argument("--chunk", type=int, default=64, choices=[64, 128])
     ap.add_argument("--beta-dtype", default="bf16", choices=["bf16", "f16", "f32"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -249,6 +250,8 @@ def main():
     if args.k_dtype != wl.k_dtype or args.beta_dtype != wl.beta_dtype:
         wl = wl.with_(k_dtype=args.k_dtype, beta_dtype=args.beta_dtype,
                       name=f"{wl.name}_k{args.k_dtype}_beta{args.beta_dtype}")
+    if args.chunk != wl.chunk:
+        wl = wl.with_(chunk=args.chunk, name=f"{wl.name}_C{args.chunk}")
     out_dtype = args.out_dtype or wl.out_dtype
     if args.impl == "reference":
         return run_reference(args, wl)
@@ -270,7 +273,7 @@ def main():
     cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].to(dev)
     odt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[out_dtype]
     codes = {"bf16": gdr.GDR_BF16, "f16": gdr.GDR_F16, "f32": gdr.GDR_F32}
-    out = torch.empty((*k.shape[:3], 64), dtype=odt, device=dev)
+    out = torch.empty((*k.shape[:3], wl.chunk), dtype=odt, device=dev)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
     B = cu.numel() - 1 if cu is not None else k.shape[0]
@@ -278,7 +281,7 @@ def main():
     def step(o=out):
         rc = gdr.kkt_solve_ex_raw(k.data_ptr(), codes[wl.k_dtype], 0 if g is None else g.data_ptr(),
                                   0 if beta is None else beta.data_ptr(), codes[wl.beta_dtype],
-                                  0 if cu is None else cu.data_ptr(), B, k.shape[1], wl.H, wl.K, 64,
+                                  0 if cu is None else cu.data_ptr(), B, k.shape[1], wl.H, wl.K, wl.chunk,
                                   codes[out_dtype], o.data_ptr(), sh)
         if rc != gdr.GDR_OK:
             raise gdr.GdrError(rc, "gdr_kkt_solve_ex")
@@ -336,7 +339,8 @@ def main():
 
     chain_steps = max(10, min(args.steps, 2000))
     chain_ms = {}
-    for name, fns in (("chain", (kkt_half, solve_half)), ("kkt", (kkt_half,)), ("solve", (solve_half,))):
+    chain_runs = (("chain", (kkt_half, solve_half)), ("kkt", (kkt_half,)), ("solve", (solve_half,)))
+    for name, fns in (chain_runs if wl.chunk == 64 else ()):
         for _ in range(3):
             for f in fns:
                 f()
@@ -353,6 +357,8 @@ def main():
     if gdr.device_status() != gdr.GDR_OK:
         raise RuntimeError("device status not ok after the unfused chain")
     del A
+    if wl.chunk != 64:
+        chain_ms = None
 
     # End to end through the public API with host buffers: H2D of the step's
     # inputs from pinned memory, the call, D2H of the full output.
@@ -370,7 +376,7 @@ def main():
             dg = None if hg is None else hg.to(dev, non_blocking=True)
             db = None if hb is None else hb.to(dev, non_blocking=True)
             dc = None if hcu is None else hcu.to(dev, non_blocking=True)
-            o = gdr.kkt_solve(dk, dg, db, dc, output_dtype=odt, stream=sh)
+            o = gdr.kkt_solve(dk, dg, db, dc, chunk_size=wl.chunk, output_dtype=odt, stream=sh)
             hout.copy_(o, non_blocking=True)
 
     for _ in range(3):
@@ -399,7 +405,7 @@ def main():
                             if args.config in PAGE_FUSED_MS and wl.K == 128 else None),
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "K": wl.K,
-                       "chunk": 64, "k": wl.k_dtype, "g": "f32", "beta": wl.beta_dtype,
+                       "chunk": wl.chunk, "k": wl.k_dtype, "g": "f32", "beta": wl.beta_dtype,
                        "out": out_dtype,
                        "compute": f"Gram {wl.k_dtype}x{wl.k_dtype}->f32 (tcgen05), gate/solve f32",
                        "l2": f"no flush: inputs+output {th_rank * bpt / 1e6:.0f} MB/step > 129 MB L2",
@@ -414,7 +420,7 @@ def main():
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,
             "clocks": clocks,
-            "unfused_chain": {
+            "unfused_chain": None if chain_ms is None else {
                 "what": "gdr_chunk_scaled_dot_kkt then gdr_solve_tril (A fp32 through HBM), same inputs",
                 "value": aggregate_value(th_rank, chain_ms["chain"], ws), "unit": UNIT,
                 "ms_per_step": chain_ms["chain"], "steps": chain_steps, "launches_per_step": 2,

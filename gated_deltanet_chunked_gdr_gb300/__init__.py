@@ -165,14 +165,15 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
     """(I + A)^{-1} of every 64-token chunk and head, on the GPU.
 
     k: bf16 or fp16 [B, T, H, K] CUDA tensor, K in {64, 128, 192, 256}
+    (K in {64, 128} for chunk_size 128)
     ([1, T, H, K] with cu_seqlens); g: fp32 [B, T, H] or None; beta: fp32,
     bf16 or fp16 [B, T, H] or None; cu_seqlens: int32 [N + 1] CUDA tensor or
     None; output_dtype: torch.float32 (default), torch.bfloat16 or
-    torch.float16.  Returns out [B, T, H, 64]."""
+    torch.float16; chunk_size: 64 or 128.  Returns out [B, T, H, chunk_size]."""
     import torch
 
-    if chunk_size != 64:
-        raise ValueError("chunk_size must be 64")
+    if chunk_size not in (64, 128):
+        raise ValueError("chunk_size must be 64 or 128")
     if output_dtype is None:
         output_dtype = torch.float32
     out_code = _gdr_dtype(output_dtype, "output_dtype")
@@ -200,8 +201,8 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
     beta = None if beta is None else beta.contiguous()
     cu_seqlens = None if cu_seqlens is None else cu_seqlens.contiguous()
     if out is None:
-        out = torch.empty((Bk, T, H, 64), dtype=output_dtype, device=k.device)
-    elif out.dtype != output_dtype or tuple(out.shape) != (Bk, T, H, 64) or not out.is_contiguous():
+        out = torch.empty((Bk, T, H, chunk_size), dtype=output_dtype, device=k.device)
+    elif out.dtype != output_dtype or tuple(out.shape) != (Bk, T, H, chunk_size) or not out.is_contiguous():
         raise ValueError("out has the wrong dtype, shape or layout")
     if stream is None:
         stream = torch.cuda.current_stream(k.device).cuda_stream

@@ -278,6 +278,12 @@ struct TileWalk {
     int64_t bn1;            // varlen: base(n + 1)
 };
 
+// CH is the chunk length (64, or 128 for the chunk-128 kernel, whose "tiles" are
+// whole chunks).
+template <int CH>
+constexpr int kLog2 = CH == 64 ? 6 : 7;
+
+template <int CH = kChunk>
 __device__ __forceinline__ TileWalk walk_init(const Params &p, uint32_t u) {
     TileWalk w;
     w.slot = p.divH.div(u);
@@ -293,7 +299,7 @@ __device__ __forceinline__ TileWalk walk_init(const Params &p, uint32_t u) {
         int64_t lo = 0, hi = p.B;
         while (lo < hi) {
             const int64_t mid = (lo + hi + 1) >> 1;
-            const int64_t bm = (static_cast<int64_t>(__ldg(p.cu + mid)) + 63 * mid) >> 6;
+            const int64_t bm = (static_cast<int64_t>(__ldg(p.cu + mid)) + (CH - 1) * mid) >> kLog2<CH>;
             if (bm <= w.slot) lo = mid;
             else hi = mid - 1;
         }
@@ -301,12 +307,13 @@ __device__ __forceinline__ TileWalk walk_init(const Params &p, uint32_t u) {
         if (lo < p.B) {
             w.s = __ldg(p.cu + lo);
             w.e = __ldg(p.cu + lo + 1);
-            w.bn1 = (static_cast<int64_t>(w.e) + 63 * (lo + 1)) >> 6;
+            w.bn1 = (static_cast<int64_t>(w.e) + (CH - 1) * (lo + 1)) >> kLog2<CH>;
         }
     }
     return w;
 }
 
+template <int CH = kChunk>
 __device__ __forceinline__ void walk_advance(const Params &p, TileWalk &w, uint32_t ds, uint32_t dh) {
     uint32_t inc = ds;
     w.h += dh;
@@ -329,12 +336,13 @@ __device__ __forceinline__ void walk_advance(const Params &p, TileWalk &w, uint3
             w.s = w.e;
             if (w.n < p.B) {
                 w.e = __ldg(p.cu + w.n + 1);
-                w.bn1 = (static_cast<int64_t>(w.e) + 63 * static_cast<int64_t>(w.n + 1)) >> 6;
+                w.bn1 = (static_cast<int64_t>(w.e) + (CH - 1) * static_cast<int64_t>(w.n + 1)) >> kLog2<CH>;
             }
         }
     }
 }
 
+template <int CH = kChunk>
 __device__ __forceinline__ Tile walk_tile(const Params &p, const TileWalk &w) {
     Tile t;
     t.row0 = 0;
@@ -342,19 +350,19 @@ __device__ __forceinline__ Tile walk_tile(const Params &p, const TileWalk &w) {
     t.h = static_cast<int>(w.h);
     if (w.slot >= static_cast<uint64_t>(p.n_slots)) return t;
     if (p.cu == nullptr) {
-        t.row0 = static_cast<int64_t>(w.b) * p.T + static_cast<int64_t>(w.c) * kChunk;
-        const int64_t rem = p.T - static_cast<int64_t>(w.c) * kChunk;
-        t.L = static_cast<int>(rem < kChunk ? rem : kChunk);
+        t.row0 = static_cast<int64_t>(w.b) * p.T + static_cast<int64_t>(w.c) * CH;
+        const int64_t rem = p.T - static_cast<int64_t>(w.c) * CH;
+        t.L = static_cast<int>(rem < CH ? rem : CH);
         return t;
     }
     if (w.n >= p.B) return t;
     const int64_t s = w.s;
     const int64_t e = w.e > p.T ? p.T : w.e;
-    const int64_t c = static_cast<int64_t>(w.slot) - ((s + 63 * static_cast<int64_t>(w.n)) >> 6);
-    const int64_t r0 = s + c * kChunk;
+    const int64_t c = static_cast<int64_t>(w.slot) - ((s + (CH - 1) * static_cast<int64_t>(w.n)) >> kLog2<CH>);
+    const int64_t r0 = s + c * CH;
     if (c < 0 || s < 0 || r0 >= e) return t;
     t.row0 = r0;
-    t.L = static_cast<int>(e - r0 < kChunk ? e - r0 : kChunk);
+    t.L = static_cast<int>(e - r0 < CH ? e - r0 : CH);
     return t;
 }
 
@@ -1122,6 +1130,473 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ chunk 128
+// (I + A)^{-1} of 128-token chunks (the chunk of the PyPTO page
+// "GatedDeltaRule算子性能优化案例", section 3.2: TileShape [128, 128]; its
+// section 3.3.2 inverts the tile through 8 blocks of 16 x 16).  A chunk is one
+// pipeline pair whose two "tiles" are its halves, so the producer, the stage
+// ring and the M = N = 128 Gram are those of the 64-token kernel, and TMEM now
+// holds all of S, including the cross block S21 (second-half rows, first-half
+// columns).  With the halves' inverses X11 = (I + A11)^{-1} and
+// X22 = (I + A22)^{-1} (the 64-token solve on each half),
+//     X = [[X11, 0], [X21, X22]],   X21 = -X22 A21 X11,
+// and X21 comes from two more block products on the tensor cores.  Two
+// consumer warpgroups (128 rows each); per warpgroup three 64 x 64 fp32
+// matrices: M0 = A11 then X11, M1 = A22 then X22, M2 = A21 then X21.
+constexpr int kC128WG = 2;
+constexpr int kC128Producer = 4 * kC128WG;
+constexpr int kC128Mma = 4 * kC128WG + 1;
+constexpr int kC128Threads = 32 * (4 * kC128WG + 2);
+constexpr int kMatBytes = kChunk * kAPitch * 4;           // 17408
+constexpr int kC128M1Off = kMatBytes + 16;                // other banks than M0
+constexpr int kC128M2Off = 2 * kMatBytes + 32;
+constexpr int kC128WGBytes = 53248;                       // >= kC128M2Off + kMatBytes, multiple of 1024
+constexpr int kC128GBytes = 2 * 2 * 128 * 4;              // g and v of 128 rows, double buffered
+constexpr int kC128OffA = kOffK + kNumStages * kStageBytes;
+constexpr int kC128OffG = kC128OffA + kC128WG * kC128WGBytes;
+constexpr int kC128OffBar = kC128OffG + kC128WG * kC128GBytes;
+constexpr int kC128OffMisc = kC128OffBar + (2 * kNumStages + 2 * kC128WG) * 8;
+constexpr int kC128SmemBytes = kC128OffMisc + 64 + 1024;
+constexpr uint32_t kC128TmemCols = 256;
+static_assert(kC128M2Off + kMatBytes <= kC128WGBytes, "chunk-128 matrices");
+static_assert(kC128SmemBytes <= 232448, "chunk-128 shared memory budget");
+
+// The half tt (0 or 1) of a 128-token chunk as a 64-row tile.
+__device__ __forceinline__ Tile half_of(const Tile &c, int tt) {
+    Tile t;
+    t.h = c.h;
+    t.row0 = c.row0 + 64 * tt;
+    const int l = c.L - 64 * tt;
+    t.L = l < 0 ? 0 : (l > 64 ? 64 : l);
+    return t;
+}
+
+template <int OUT, int NKB>
+__global__ void __launch_bounds__(kC128Threads, 1)
+    kkt_solve_c128_kernel(const __grid_constant__ CUtensorMap tmap_k, const Params p) {
+    constexpr bool SPLIT = OUT != kOutBF16;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + kC128OffBar;                   // [kNumStages]
+    const uint32_t bar_empty = bar_full + 8 * kNumStages;            // [kNumStages]
+    const uint32_t bar_tfull = bar_empty + 8 * kNumStages;           // [kC128WG]
+    const uint32_t bar_tempty = bar_tfull + 8 * kC128WG;             // [kC128WG]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kC128OffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kC128OffMisc + 4);
+    volatile int *wg_flag = reinterpret_cast<volatile int *>(smem + kC128OffMisc + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNumStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int w = 0; w < kC128WG; ++w) {
+            mbar_init(bar_tfull + 8 * w, 1);
+            mbar_init(bar_tempty + 8 * w, 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kC128Mma) {
+        tmem_alloc(smem_u32(tmem_slot), kC128TmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int64_t n_local = (p.n_pairs > blockIdx.x)
+                                ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
+                                : 0;
+    constexpr int nkb = NKB;
+    constexpr int nkc = (nkb + 1) >> 1;
+
+    if (warp == kC128Producer) {
+        // As in the 64-token kernel; lane tt & 1 issues the copies of half tt.
+        if (lane < 4) {
+            if (lane == 0)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
+                             : "memory");
+            const int tt = lane & 1;
+            const bool pf_lane = lane >= 2;
+            TileWalk w = walk_init<128>(p, static_cast<uint32_t>(blockIdx.x));
+            if (pf_lane)
+                for (int i = 0; i < kPrefetchPairs; ++i) walk_advance<128>(p, w, p.pair_ds, p.pair_dh);
+            int64_t q = 0;
+            int kc = 0;
+            bool failed = false;
+            for (; q < n_local; ++q) {
+                int stop = (lane == 0) ? *abort_flag : 0;
+                if (__shfl_sync(0xFu, stop, 0)) break;
+                const Tile t = half_of(walk_tile<128>(p, w), tt);
+                if (pf_lane) {
+                    if (q + kPrefetchPairs < n_local) {
+                        if (t.L > 0)
+#pragma unroll
+                            for (int kb = 0; kb < nkb; ++kb)
+                                tma_prefetch_3d(&tmap_k, 64 * kb, t.h, static_cast<int>(t.row0));
+                        walk_advance<128>(p, w, p.pair_ds, p.pair_dh);
+                    }
+                } else if (q + 1 < n_local) {
+                    walk_advance<128>(p, w, p.pair_ds, p.pair_dh);
+                }
+                const uint32_t loads = __ballot_sync(0xFu, !pf_lane && t.L > 0) & 3u;
+#pragma unroll
+                for (kc = 0; kc < nkc; ++kc) {
+                    const int64_t v = q * nkc + kc;
+                    const int nb = (2 * kc + 1 < nkb) ? 2 : 1;
+                    const int s = static_cast<int>(v % kNumStages);
+                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                    const uint32_t st = sbase + kOffK + s * kStageBytes;
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = mbar_wait(bar_empty + 8 * s, ph ^ 1) ? 1 : 0;
+                        if (!ok) record_timeout(p, abort_flag);
+                        else mbar_arrive_expect_tx(bar_full + 8 * s, __popc(loads) * nb * kBoxBytes);
+                    }
+                    if (!__shfl_sync(0xFu, ok, 0)) {
+                        failed = true;
+                        break;
+                    }
+                    if (!pf_lane && t.L > 0)
+#pragma unroll
+                        for (int kh = 0; kh < nb; ++kh)
+                            tma_load_3d(st + (2 * kh + tt) * kBoxBytes, &tmap_k, bar_full + 8 * s,
+                                        64 * (2 * kc + kh), t.h, static_cast<int>(t.row0));
+                }
+                if (failed) break;
+            }
+            const int64_t v = q * nkc + (failed ? kc : 0);
+            if (lane == 0) {
+                const int64_t first = v > kNumStages ? v - kNumStages : 0;
+                for (int64_t r = first; r < v; ++r) {
+                    const int s = static_cast<int>(r % kNumStages);
+                    const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
+                    if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
+                    if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
+                }
+            }
+        }
+    } else if (warp == kC128Mma) {
+        if (lane == 0) {
+            int64_t q = 0;
+            bool failed = false;
+            for (; q < n_local; ++q) {
+                if (*abort_flag) break;
+                const int w = static_cast<int>(q % kC128WG);
+                const uint32_t phw = static_cast<uint32_t>((q / kC128WG) & 1);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w);
+#pragma unroll
+                for (int kc = 0; kc < nkc; ++kc) {
+                    const int64_t v = q * nkc + kc;
+                    const int s = static_cast<int>(v % kNumStages);
+                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                    if (!mbar_wait(bar_full + 8 * s, ph) ||
+                        (kc == 0 && !mbar_wait(bar_tempty + 8 * w, phw ^ 1))) {
+                        record_timeout(p, abort_flag);
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = sbase + kOffK + s * kStageBytes;
+                    const int nb = (2 * kc + 1 < nkb) ? 2 : 1;
+#pragma unroll
+                    for (int kh = 0; kh < nb; ++kh) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
+                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(a_addr), p.idesc,
+                                       (kc | kh | ks) ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(bar_empty + 8 * s);
+                    if (kc == nkc - 1) tc_commit(bar_tfull + 8 * w);
+                }
+                if (failed) break;
+            }
+            if (q > 0) {
+                const int64_t r = q - 1;
+                const int w = static_cast<int>(r % kC128WG);
+                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kC128WG) & 1)))
+                    record_timeout(p, abort_flag);
+            }
+        }
+    } else {
+        // ------------------------------------------------ consumer warpgroups
+        const int wg = warp >> 2;
+        const int qd = warp & 3;
+        const int i = 32 * qd + lane;            // row of the chunk = TMEM lane
+        const int hf = qd >> 1;                  // half of this row
+        const int ih = i & 63;                   // row within the half
+        const int tid = threadIdx.x & 127;
+        const int g8 = lane >> 2, t4 = lane & 3;
+        uint8_t *mb = smem + kC128OffA + wg * kC128WGBytes;
+        float *const M0 = reinterpret_cast<float *>(mb);
+        float *const M1 = reinterpret_cast<float *>(mb + kC128M1Off);
+        float *const M2 = reinterpret_cast<float *>(mb + kC128M2Off);
+        auto Mh = [M0, M1](int t) { return t ? M1 : M0; };
+        auto blk = [](float *M, int I, int J) { return M + 16 * I * kAPitch + 16 * J; };
+        float *gbuf = reinterpret_cast<float *>(smem + kC128OffG + wg * kC128GBytes);   // [parity][128]
+        float *vbuf = gbuf + 2 * 128;
+        const int bar_id = 1 + wg;
+
+        int64_t q = wg;
+        TileWalk wk = walk_init<128>(p, static_cast<uint32_t>(blockIdx.x + q * gridDim.x));
+        Tile cur = walk_tile<128>(p, wk);
+        RowIn rin = load_row(p, cur, i);
+
+        for (int r = 0; q < n_local; ++r, q += kC128WG) {
+            const int64_t qn = q + kC128WG;
+            Tile nx;
+            nx.L = 0;
+            nx.row0 = 0;
+            nx.h = 0;
+            if (qn < n_local) {
+                walk_advance<128>(p, wk, p.wg_ds, p.wg_dh);
+                nx = walk_tile<128>(p, wk);
+            }
+            const RowIn rnext = load_row(p, nx, i);
+
+            if (qd == 3 && lane == 0) {
+                int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
+                if (!ok) record_timeout(p, abort_flag);
+                wg_flag[wg] = ok;
+            }
+            // Gate factors around the whole chunk's reference (the cross block
+            // needs one reference for both halves); same safety rule as for 64.
+            const bool rowok = i < cur.L;
+            float ui = 1.0f, vi = 1.0f;
+            bool unsafe = false;
+            if (p.g && rowok) {
+                const float dg = rin.g - 0.5f * (rin.gfirst + rin.glast);
+                unsafe = !(fabsf(dg) <= 30.0f);
+                ui = expf(dg);
+                vi = expf(-dg);
+            }
+            float *gcur = gbuf + (r & 1) * 128;
+            float *vcur = vbuf + (r & 1) * 128;
+            gcur[i] = rin.g;
+            vcur[i] = rowok ? vi : 0.0f;
+            const bool direct = named_bar_red_or(bar_id, 128, unsafe);   // g, v ready; matrices free
+            if (!wg_flag[wg]) break;
+            tc_fence_after();
+
+            // ---- epilogue: the diagonal block row into M0 / M1 and, for second-half
+            //      rows, the cross block row into M2
+            {
+                const float bi = beta_value(p, rin.beta);
+                const float w = bi * ui;
+                const float gi = rin.g;
+                const int npass = hf ? 2 : 1;
+                for (int pass = 0; pass < npass; ++pass) {
+                    const int cb = pass == 0 ? 64 * hf : 0;        // TMEM columns = partner rows
+                    uint32_t sr[64];
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
+                                           static_cast<uint32_t>(128 * wg + cb);
+                    {
+                        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
+                        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
+                        tmem_ld32(taddr, lo);
+                        tmem_ld32(taddr + 32, hi);
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) reg_fence(sr[j]);
+                    float4 *Arow = reinterpret_cast<float4 *>((pass == 0 ? Mh(hf) : M2) + ih * kAPitch);
+                    // Diagonal block rows 0..31 only need columns j < 32.
+                    const int n4 = (pass == 1 || (qd & 1)) ? 16 : 8;
+                    const float4 *vj = reinterpret_cast<const float4 *>(vcur + cb);
+                    const float4 *gj = reinterpret_cast<const float4 *>(gcur + cb);
+                    if (!rowok) {
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int j4 = 0; j4 < 16; ++j4)
+                            if (j4 < n4) Arow[j4] = z;
+                    } else if (!direct) {
+#pragma unroll
+                        for (int j4 = 0; j4 < 16; ++j4) {
+                            if (j4 < n4) {
+                                const float4 v = vj[j4];
+                                float4 a;
+                                a.x = (__uint_as_float(sr[4 * j4 + 0]) * w) * v.x;
+                                a.y = (__uint_as_float(sr[4 * j4 + 1]) * w) * v.y;
+                                a.z = (__uint_as_float(sr[4 * j4 + 2]) * w) * v.z;
+                                a.w = (__uint_as_float(sr[4 * j4 + 3]) * w) * v.w;
+                                Arow[j4] = a;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j4 = 0; j4 < 16; ++j4) {
+                            if (j4 < n4) {
+                                const float4 gg = gj[j4];
+                                float4 a;
+                                a.x = bi * __uint_as_float(sr[4 * j4 + 0]) * __expf(fminf(fmaxf(gi - gg.x, -50.f), 50.f));
+                                a.y = bi * __uint_as_float(sr[4 * j4 + 1]) * __expf(fminf(fmaxf(gi - gg.y, -50.f), 50.f));
+                                a.z = bi * __uint_as_float(sr[4 * j4 + 2]) * __expf(fminf(fmaxf(gi - gg.z, -50.f), 50.f));
+                                a.w = bi * __uint_as_float(sr[4 * j4 + 3]) * __expf(fminf(fmaxf(gi - gg.w, -50.f), 50.f));
+                                Arow[j4] = a;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
+            }
+            // A warp's diagonal blocks are the 32 rows it has just written.
+            __syncwarp();
+
+            // ---- diagonal inverses: thread -> (half, block, row) as in the 64 kernel
+            const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
+            float drow[16];
+            diag_inverse_row(Mh(dt) + 16 * dI * (kAPitch + 1), dc, drow);
+            {
+                float4 *dst = reinterpret_cast<float4 *>(Mh(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
+                                                         16 * dslot_c(dI));
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4)
+                    dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
+            }
+            named_bar_sync(bar_id, 128);                       // D blocks ready
+
+            // ---- X11 and X22: the 64-token merge on each half, then written out as
+            //      fp32 rows (diagonal blocks from the substitution rows)
+            const int mt = qd & 1;
+            if (qd < 2) {
+                float z0[3][2][4];
+                merge_column<0, SPLIT>(Mh(mt), g8, t4, z0);
+                named_bar_sync(bar_id, 128);                   // A11, A22 no longer read
+                store_block_T(Mh(mt), 1, 0, z0[0], g8, t4);
+                store_block_T(Mh(mt), 2, 0, z0[1], g8, t4);
+                store_block_T(Mh(mt), 3, 0, z0[2], g8, t4);
+            } else {
+                float z1[2][2][4], z2[1][2][4];
+                merge_column<1, SPLIT>(Mh(mt), g8, t4, z1);
+                merge_column<2, SPLIT>(Mh(mt), g8, t4, z2);
+                named_bar_sync(bar_id, 128);                   // A11, A22 no longer read
+                store_block_T(Mh(mt), 2, 1, z1[0], g8, t4);
+                store_block_T(Mh(mt), 3, 1, z1[1], g8, t4);
+                store_block_T(Mh(mt), 3, 2, z2[0], g8, t4);
+            }
+            {
+                float4 *dst = reinterpret_cast<float4 *>(Mh(dt) + (16 * dI + dc) * kAPitch + 16 * dI);
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4)
+                    dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
+            }
+            named_bar_sync(bar_id, 128);                       // X11, X22 complete
+
+            // ---- X21 = -X22 (A21 X11), warp -> block column J, transposed as in
+            //      the merge: P_MJ^T = sum_{K>=J} X11_KJ^T A21_MK^T, then
+            //      X21_IJ^T = -sum_{M<=I} P_MJ^T X22_IM^T.
+            {
+                const int J = qd;
+                float pt[4][2][4];
+#pragma unroll
+                for (int M = 0; M < 4; ++M) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) pt[M][nt][e] = 0.0f;
+                    for (int K2 = J; K2 < 4; ++K2) {
+                        Frag16 f;
+                        frag_from_dT<SPLIT>(blk(M0, K2, J), g8, t4, f);
+                        mma3_times_blockT<SPLIT>(pt[M], f, blk(M2, M, K2), g8, t4);
+                    }
+                }
+                named_bar_sync(bar_id, 128);                   // A21 no longer read
+#pragma unroll
+                for (int I = 0; I < 4; ++I) {
+                    float acc[2][4] = {};
+#pragma unroll
+                    for (int M = 0; M < 4; ++M) {
+                        if (M <= I) {
+                            Frag16 f;
+                            frag_from_acc<SPLIT>(pt[M], f);
+                            mma3_times_blockT<SPLIT>(acc, f, blk(M1, I, M), g8, t4);
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[nt][e] = -acc[nt][e];
+                    store_block_T(M2, I, J, acc, g8, t4);
+                }
+            }
+            named_bar_sync(bar_id, 128);                       // X complete
+
+            // ---- store: every row of the chunk, 128 values; lower triangle of
+            //      X11 / X22 (masked), X21 in full, zeros elsewhere
+            {
+                char *const ob = reinterpret_cast<char *>(p.out);
+                constexpr int kEsz = OUT == kOutF32 ? 4 : 2;
+                constexpr int kRowsPerIt = OUT == kOutF32 ? 1 : 2;
+                constexpr int kCols = OUT == kOutF32 ? 4 : 8;   // values per lane
+                const int sub = lane / (32 / kRowsPerIt);
+                const int cl = lane % (32 / kRowsPerIt);
+                const int c0 = cl * kCols;                      // first column of this lane
+#pragma unroll 4
+                for (int it = 0; it < 32 / kRowsPerIt; ++it) {
+                    const int rr = 32 * qd + kRowsPerIt * it + sub;
+                    if (rr >= cur.L) continue;
+                    const int rh = rr & 63;
+                    float v[kCols];
+                    const bool right = c0 >= 64;
+                    const int cc = c0 & 63;
+                    const float *src;
+                    bool zero = false, mask = true;
+                    if (rr < 64) {
+                        src = M0 + rh * kAPitch + cc;
+                        zero = right;
+                    } else if (!right) {
+                        src = M2 + rh * kAPitch + cc;
+                        mask = false;
+                    } else {
+                        src = M1 + rh * kAPitch + cc;
+                    }
+#pragma unroll
+                    for (int e4 = 0; e4 < kCols / 4; ++e4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(src + 4 * e4);
+                        v[4 * e4 + 0] = x.x;
+                        v[4 * e4 + 1] = x.y;
+                        v[4 * e4 + 2] = x.z;
+                        v[4 * e4 + 3] = x.w;
+                    }
+#pragma unroll
+                    for (int e = 0; e < kCols; ++e)
+                        if (zero || (mask && cc + e > rh)) v[e] = 0.0f;
+                    char *dst = ob + ((cur.row0 + rr) * p.H + cur.h) * (128 * kEsz) + c0 * kEsz;
+                    if (OUT == kOutF32) {
+                        *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
+                        uint4 u;
+                        u.x = pack16x2<OUT>(v[0], v[1]);
+                        u.y = pack16x2<OUT>(v[2], v[3]);
+                        u.z = pack16x2<OUT>(v[4 % kCols], v[5 % kCols]);
+                        u.w = pack16x2<OUT>(v[6 % kCols], v[7 % kCols]);
+                        *reinterpret_cast<uint4 *>(dst) = u;
+                    }
+                }
+            }
+            cur = nx;
+            rin = rnext;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kC128Mma) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kC128TmemCols);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
@@ -1138,6 +1613,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 using KernelFn = void (*)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap, Params);
+using KernelFn128 = void (*)(const __grid_constant__ CUtensorMap, Params);
 
 template <int OUT, int MODE>
 KernelFn kernel_for_nkb(int nkb) {
@@ -1147,6 +1623,12 @@ KernelFn kernel_for_nkb(int nkb) {
         case 3: return kkt_solve_kernel<OUT, 3, MODE>;
         default: return kkt_solve_kernel<OUT, 4, MODE>;
     }
+}
+
+KernelFn128 kernel_c128_for(int out_kind, int nkb) {
+    if (out_kind == kOutBF16) return nkb == 1 ? kkt_solve_c128_kernel<kOutBF16, 1> : kkt_solve_c128_kernel<kOutBF16, 2>;
+    if (out_kind == kOutF16) return nkb == 1 ? kkt_solve_c128_kernel<kOutF16, 1> : kkt_solve_c128_kernel<kOutF16, 2>;
+    return nkb == 1 ? kkt_solve_c128_kernel<kOutF32, 1> : kkt_solve_c128_kernel<kOutF32, 2>;
 }
 
 // The instantiation for a mode, an output kind (gdr_dtype value) and K / 64.
@@ -1224,6 +1706,11 @@ int prepare_device(int *sms) {
                     attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(m, o, n),
                                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                               kSmemBytes) == cudaSuccess;
+        for (int o = 0; o < 3; ++o)
+            for (int n = 1; n <= 2; ++n)
+                attr_ok = attr_ok && cudaFuncSetAttribute(kernel_c128_for(o, n),
+                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                          kC128SmemBytes) == cudaSuccess;
         if (!attr_ok) {
             cudaGetLastError();
             return GDR_ERR_CUDA;
@@ -1270,7 +1757,9 @@ namespace gdr {
 int validate(int mode, const void *in, int in_dtype, const void *g, const void *beta, int beta_dtype,
              const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size,
              int out_dtype, const void *out) {
-    if (chunk_size != kChunk) return GDR_ERR_CHUNK;
+    // Chunk 128: the fused call only, K = 64 or 128.
+    if (chunk_size != kChunk && !(chunk_size == 128 && mode == kModeFused)) return GDR_ERR_CHUNK;
+    if (chunk_size == 128 && K > 128) return GDR_ERR_SHAPE;
     if (mode == kModeSolve ? in_dtype != GDR_F32 : (in_dtype != GDR_BF16 && in_dtype != GDR_F16))
         return GDR_ERR_DTYPE;
     if (beta && beta_dtype != GDR_F32 && beta_dtype != GDR_BF16 && beta_dtype != GDR_F16)
@@ -1329,7 +1818,7 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     }
     const int out_kind = mode == kModeKkt ? GDR_F32 : out_dtype;
     CUtensorMap tmap_o;
-    {
+    if (chunk_size == kChunk) {     // the chunk-128 kernel stores rows without TMA
         const int esz = out_kind == GDR_F32 ? 4 : 2;
         const CUtensorMapDataType odt = out_kind == GDR_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                         : out_kind == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -1354,10 +1843,11 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     prm.B = B;
     prm.T = T;
     prm.H = H;
-    prm.NT = (T + kChunk - 1) / kChunk;
-    prm.n_slots = cu_seqlens ? (T + 63 * B) / kChunk : B * prm.NT;
+    const int64_t CH = chunk_size;                 // 64, or 128 (one chunk per pipeline pair)
+    prm.NT = (T + CH - 1) / CH;
+    prm.n_slots = cu_seqlens ? (T + (CH - 1) * B) / CH : B * prm.NT;
     if (prm.n_slots * H >= (int64_t(1) << 31)) return GDR_ERR_SHAPE;
-    prm.n_pairs = (prm.n_slots * H + 1) / 2;
+    prm.n_pairs = CH == 128 ? prm.n_slots * H : (prm.n_slots * H + 1) / 2;
     prm.divH = make_fastdiv(static_cast<uint32_t>(H));
     prm.divNT = make_fastdiv(static_cast<uint32_t>(prm.NT));
     int *status_ptr = nullptr;
@@ -1368,12 +1858,20 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     prm.status = status_ptr;
 
     const int64_t grid = prm.n_pairs < sms ? prm.n_pairs : sms;
-    prm.pair_ds = static_cast<uint32_t>((2 * grid) / H);
-    prm.pair_dh = static_cast<uint32_t>((2 * grid) % H);
-    prm.wg_ds = static_cast<uint32_t>((2 * grid * kNumWG) / H);
-    prm.wg_dh = static_cast<uint32_t>((2 * grid * kNumWG) % H);
+    // Tile strides of a CTA's and of a warpgroup's consecutive pairs.
+    const int64_t per_pair = CH == 128 ? 1 : 2;
+    const int64_t n_wg = CH == 128 ? kC128WG : kNumWG;
+    prm.pair_ds = static_cast<uint32_t>((per_pair * grid) / H);
+    prm.pair_dh = static_cast<uint32_t>((per_pair * grid) % H);
+    prm.wg_ds = static_cast<uint32_t>((per_pair * grid * n_wg) / H);
+    prm.wg_dh = static_cast<uint32_t>((per_pair * grid * n_wg) % H);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned gx = static_cast<unsigned>(grid);
+    if (CH == 128) {
+        kernel_c128_for(out_kind, static_cast<int>(K / 64))<<<gx, kC128Threads, kC128SmemBytes, st>>>(tmap, prm);
+        if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+        return GDR_OK;
+    }
     kernel_for(mode, out_kind, static_cast<int>(K / 64))<<<gx, kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;

@@ -53,9 +53,20 @@ def _call(**kw):
                              a["chunk"], a["dtype"], a["out"], 0)
 
 
-@pytest.mark.parametrize("chunk", [0, 16, 32, 63, 65, 128])
-def test_chunk_size_must_be_64(chunk):
+@pytest.mark.parametrize("chunk", [0, 16, 32, 63, 65, 96, 256])
+def test_chunk_size_must_be_64_or_128(chunk):
     assert _call(chunk=chunk) == gdr.GDR_ERR_CHUNK
+
+
+def test_chunk_128_limits():
+    import torch
+    assert _call(chunk=128, K=192) == gdr.GDR_ERR_SHAPE          # chunk 128 takes K <= 128
+    assert _call_kkt(chunk=128) == gdr.GDR_ERR_CHUNK             # the unfused chain is chunk 64 only
+    assert _call_solve(chunk=128) == gdr.GDR_ERR_CHUNK
+    assert _call_noalloc(chunk=128) == gdr.GDR_ERR_CHUNK
+    if not torch.cuda.is_available():
+        assert _call(chunk=128) == gdr.GDR_ERR_DEVICE
+        assert _call(chunk=128, K=64) == gdr.GDR_ERR_DEVICE
 
 
 @pytest.mark.parametrize("dtype", [-1, 3, 7])
@@ -136,6 +147,8 @@ def test_python_binding_rejects_chunk_size_like_the_page_api():
     k = torch.zeros(1, 64, 1, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         gdr.kkt_solve(k, chunk_size=32)
+    with pytest.raises(ValueError):
+        gdr.solve_tril(torch.zeros(1, 64, 1, 64), chunk_size=128)
     with pytest.raises(TypeError):
         gdr.kkt_solve(k)                       # CPU tensor: no CPU fallback exists
 

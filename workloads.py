@@ -45,6 +45,7 @@ class Workload:
     use_beta: bool = True
     k_dtype: str = "bf16"       # "bf16" or "f16": type k is rounded to
     beta_dtype: str = "bf16"    # "bf16", "f16" or "f32"
+    chunk: int = CHUNK          # chunk length the log-gate's running sum restarts at
 
     @property
     def token_heads(self) -> int:
@@ -93,12 +94,12 @@ def _sequence_bounds(wl: Workload):
     return [(int(cu[n]), int(cu[n + 1])) for n in range(wl.B)]
 
 
-def _chunk_local_cumsum(a: np.ndarray, bounds) -> np.ndarray:
+def _chunk_local_cumsum(a: np.ndarray, bounds, chunk: int = CHUNK) -> np.ndarray:
     """Inclusive running sum of a [Ntok, H] restarted at every chunk start."""
     g = np.empty_like(a)
     for s, e in bounds:
-        for c0 in range(s, e, CHUNK):
-            c1 = min(c0 + CHUNK, e)
+        for c0 in range(s, e, chunk):
+            c1 = min(c0 + chunk, e)
             g[c0:c1] = np.cumsum(a[c0:c1], axis=0, dtype=np.float32)
     return g
 
@@ -119,7 +120,7 @@ def make_inputs(wl: Workload):
         k[r0:r1] = x
     beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((ntok, H), dtype=np.float32)))
     a = -0.1 * rng.random((ntok, H), dtype=np.float32)
-    g = _chunk_local_cumsum(a.astype(np.float32), _sequence_bounds(wl))
+    g = _chunk_local_cumsum(a.astype(np.float32), _sequence_bounds(wl), wl.chunk)
 
     lead = (wl.B, wl.T) if wl.varlen_lengths is None else (1, wl.T)
     types = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
@@ -140,11 +141,11 @@ def make_inputs(wl: Workload):
 def tile_list(wl: Workload):
     """All (sequence, chunk, head) tiles of a workload with their token ranges:
     list of (n, c, h, row0, L) where row0 is the first token row of the chunk in
-    the flattened token axis and L <= 64 its length."""
+    the flattened token axis and L <= wl.chunk its length."""
     tiles = []
     for n, (s, e) in enumerate(_sequence_bounds(wl)):
-        for c, r0 in enumerate(range(s, e, CHUNK)):
-            L = min(CHUNK, e - r0)
+        for c, r0 in enumerate(range(s, e, wl.chunk)):
+            L = min(wl.chunk, e - r0)
             for h in range(wl.H):
                 tiles.append((n, c, h, r0, L))
     return tiles
