@@ -165,7 +165,8 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
     """(I + A)^{-1} of every 64-token chunk and head, on the GPU.
 
     k: bf16 or fp16 [B, T, H, K] CUDA tensor, K in {64, 128, 192, 256}
-    (K in {64, 128} for chunk_size 128)
+    (K in {64, 128} for chunk_size 128), or fp32 with K in {64, 128} and
+    chunk_size 64
     ([1, T, H, K] with cu_seqlens); g: fp32 [B, T, H] or None; beta: fp32,
     bf16 or fp16 [B, T, H] or None; cu_seqlens: int32 [N + 1] CUDA tensor or
     None; output_dtype: torch.float32 (default), torch.bfloat16 or
@@ -177,8 +178,8 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
     if output_dtype is None:
         output_dtype = torch.float32
     out_code = _gdr_dtype(output_dtype, "output_dtype")
-    if k.dtype not in (torch.bfloat16, torch.float16) or k.dim() != 4 or not k.is_cuda:
-        raise TypeError("k must be a 4-D bf16 or fp16 CUDA tensor")
+    if k.dtype not in (torch.bfloat16, torch.float16, torch.float32) or k.dim() != 4 or not k.is_cuda:
+        raise TypeError("k must be a 4-D bf16, fp16 or fp32 CUDA tensor")
     k_code = _gdr_dtype(k.dtype, "k")
     beta_code = GDR_F32 if beta is None else _gdr_dtype(beta.dtype, "beta")
     for name, t, dt in (("g", g, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)):

@@ -215,6 +215,15 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -255,6 +264,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 }
 // Instruction descriptor, kind::f16: D fp32, A and B of the key type (format 1 =
 // bf16, 0 = fp16), both K-major, N = 128, M = 128.
+// kind::tf32: D fp32, A and B tf32 (format 2), both K-major, N = 128, M = 128.
+constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t idesc_f16_kind(bool bf16_keys) {
     return (1u << 4) | ((bf16_keys ? 1u : 0u) << 7) | ((bf16_keys ? 1u : 0u) << 10) |
            ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -698,6 +709,12 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
 // halves run the fused step's own code, so the two-kernel chain reproduces the
 // fused result bit for bit.
 constexpr int kModeFused = 0, kModeKkt = 1, kModeSolve = 2;
+// The fused step with fp32 keys: the stage unit is one 32-column fp32 box per
+// tile (NKB = K / 32 units per pair); the MMA warp splits each unit into
+// big = x with the 13 low mantissa bits cleared (exact in tf32) and
+// small = x - big, and the Gram is big big^T + big small^T + small big^T on the
+// kind::tf32 tensor cores (the dropped small small^T is below 2^-20 relative).
+constexpr int kModeF32Keys = 3;
 
 // OUT: kOutF32, kOutBF16 or kOutF16.  The merge runs split (fp32-accurate) for
 // fp32 and fp16 output and as one tf32 pass for bf16 output.  NKB = K / 64, the
@@ -712,7 +729,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     static_assert(MODE != kModeKkt || OUT == kOutF32, "A is written as fp32");
     static_assert(MODE != kModeSolve || NKB == 2, "an A tile row is two 128-byte boxes");
     constexpr bool kUseTmem = MODE != kModeSolve;
-    constexpr int kBoxCols = MODE == kModeSolve ? 32 : 64;   // elements per 128-byte box row
+    constexpr bool kF32Keys = MODE == kModeF32Keys;
+    // Elements per 128-byte box row: 64 bf16/fp16 key columns, or 32 fp32 ones.
+    constexpr int kBoxCols = (MODE == kModeSolve || kF32Keys) ? 32 : 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -759,7 +778,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // unit per pair, K = 192 or 256 two.  A unit holds one or two 64-column boxes
     // of each of the pair's tiles; the Gram accumulates over a pair's units.
     constexpr int nkb = NKB;
-    constexpr int nkc = (nkb + 1) >> 1;
+    constexpr int nkc = kF32Keys ? nkb : (nkb + 1) >> 1;
     if (warp == kProducerWarp) {
         // Lanes 0 and 1 walk the two tiles of pair q (loaded into the stage ring),
         // lanes 2 and 3 those of pair q + kPrefetchPairs (prefetched into L2).
@@ -796,7 +815,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                 for (kc = 0; kc < nkc; ++kc) {
                     const int64_t v = q * nkc + kc;
-                    const int nb = (2 * kc + 1 < nkb) ? 2 : 1;
+                    const int nb = kF32Keys ? 1 : ((2 * kc + 1 < nkb) ? 2 : 1);
+                    const int box0 = kF32Keys ? kc : 2 * kc;
                     const int s = static_cast<int>(v % kNumStages);
                     const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
                     const uint32_t st = sbase + kOffK + s * kStageBytes;
@@ -814,7 +834,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                         for (int kh = 0; kh < nb; ++kh)
                             tma_load_3d(st + (2 * kh + tt) * kBoxBytes, &tmap_k, bar_full + 8 * s,
-                                        kBoxCols * (2 * kc + kh), t.h, static_cast<int>(t.row0));
+                                        kBoxCols * (box0 + kh), t.h, static_cast<int>(t.row0));
                 }
                 if (failed) break;
             }
@@ -829,6 +849,74 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
                 }
             }
+        }
+    } else if (kF32Keys && warp == kMmaWarp) {
+        // The whole warp splits each unit; lane 0 waits and issues the MMAs.
+        int64_t q = 0;
+        bool failed = false;
+        for (; q < n_local; ++q) {
+            if (*abort_flag) break;
+            const int w = static_cast<int>(q % kNumWG);
+            const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
+            const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w);
+            for (int kc = 0; kc < nkc; ++kc) {
+                const int64_t v = q * nkc + kc;
+                const int s = static_cast<int>(v % kNumStages);
+                const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                int ok = 1;
+                if (lane == 0)
+                    ok = (mbar_wait(bar_full + 8 * s, ph) &&
+                          (kc != 0 || mbar_wait(bar_tempty + 8 * w, phw ^ 1))) ? 1 : 0;
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+                    if (lane == 0) record_timeout(p, abort_flag);
+                    failed = true;
+                    break;
+                }
+                // Split the unit's two 64 x 32 fp32 boxes (16 KB) in place; the
+                // small parts go to the stage's second half.
+                float4 *const big = reinterpret_cast<float4 *>(smem + kOffK + s * kStageBytes);
+                float4 *const small = big + 2 * kBoxBytes / 16;
+#pragma unroll 4
+                for (int it = 0; it < 2 * kBoxBytes / 16 / 32; ++it) {
+                    const int idx = lane + 32 * it;
+                    const float4 x = big[idx];
+                    float4 b, m;
+                    b.x = __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+                    b.y = __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+                    b.z = __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+                    b.w = __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+                    m.x = x.x - b.x;
+                    m.y = x.y - b.y;
+                    m.z = x.z - b.z;
+                    m.w = x.w - b.w;
+                    big[idx] = b;
+                    small[idx] = m;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t st = sbase + kOffK + s * kStageBytes;
+                    const uint32_t sm = st + 2 * kBoxBytes;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t db = smem_desc_sw128(st + ks * 32), dm = smem_desc_sw128(sm + ks * 32);
+                        tc_mma_tf32(d, db, db, p.idesc, (kc | ks) ? 1u : 0u);
+                        tc_mma_tf32(d, db, dm, p.idesc, 1u);
+                        tc_mma_tf32(d, dm, db, p.idesc, 1u);
+                    }
+                    tc_commit(bar_empty + 8 * s);
+                    if (kc == nkc - 1) tc_commit(bar_tfull + 8 * w);
+                }
+                __syncwarp();
+            }
+            if (failed) break;
+        }
+        if (lane == 0 && q > 0) {
+            const int64_t r = q - 1;
+            const int w = static_cast<int>(r % kNumWG);
+            if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
+                record_timeout(p, abort_flag);
         }
     } else if (warp == kMmaWarp) {
         if (kUseTmem && lane == 0) {
@@ -1639,6 +1727,11 @@ KernelFn kernel_for(int mode, int out_kind, int nkb) {
         if (out_kind == kOutF16) return kkt_solve_kernel<kOutF16, 2, kModeSolve>;
         return kkt_solve_kernel<kOutF32, 2, kModeSolve>;
     }
+    if (mode == kModeF32Keys) {   // nkb = K / 32: 2 or 4
+        if (out_kind == kOutBF16) return nkb == 2 ? kkt_solve_kernel<kOutBF16, 2, kModeF32Keys> : kkt_solve_kernel<kOutBF16, 4, kModeF32Keys>;
+        if (out_kind == kOutF16) return nkb == 2 ? kkt_solve_kernel<kOutF16, 2, kModeF32Keys> : kkt_solve_kernel<kOutF16, 4, kModeF32Keys>;
+        return nkb == 2 ? kkt_solve_kernel<kOutF32, 2, kModeF32Keys> : kkt_solve_kernel<kOutF32, 4, kModeF32Keys>;
+    }
     if (out_kind == kOutBF16) return kernel_for_nkb<kOutBF16, kModeFused>(nkb);
     if (out_kind == kOutF16) return kernel_for_nkb<kOutF16, kModeFused>(nkb);
     return kernel_for_nkb<kOutF32, kModeFused>(nkb);
@@ -1707,6 +1800,11 @@ int prepare_device(int *sms) {
                                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                               kSmemBytes) == cudaSuccess;
         for (int o = 0; o < 3; ++o)
+            for (int n = 2; n <= 4; n += 2)
+                attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(kModeF32Keys, o, n),
+                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                          kSmemBytes) == cudaSuccess;
+        for (int o = 0; o < 3; ++o)
             for (int n = 1; n <= 2; ++n)
                 attr_ok = attr_ok && cudaFuncSetAttribute(kernel_c128_for(o, n),
                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1760,8 +1858,13 @@ int validate(int mode, const void *in, int in_dtype, const void *g, const void *
     // Chunk 128: the fused call only, K = 64 or 128.
     if (chunk_size != kChunk && !(chunk_size == 128 && mode == kModeFused)) return GDR_ERR_CHUNK;
     if (chunk_size == 128 && K > 128) return GDR_ERR_SHAPE;
-    if (mode == kModeSolve ? in_dtype != GDR_F32 : (in_dtype != GDR_BF16 && in_dtype != GDR_F16))
+    // Keys: bf16 or fp16; fp32 keys for the fused chunk-64 call only (K = 64 or 128).
+    const bool f32_keys = mode == kModeFused && in_dtype == GDR_F32;
+    if (mode == kModeSolve ? in_dtype != GDR_F32
+                           : (in_dtype != GDR_BF16 && in_dtype != GDR_F16 && !f32_keys))
         return GDR_ERR_DTYPE;
+    if (f32_keys && chunk_size != kChunk) return GDR_ERR_DTYPE;
+    if (f32_keys && K > 128) return GDR_ERR_SHAPE;
     if (beta && beta_dtype != GDR_F32 && beta_dtype != GDR_BF16 && beta_dtype != GDR_F16)
         return GDR_ERR_DTYPE;
     if (out_dtype != GDR_F32 && out_dtype != GDR_BF16 && out_dtype != GDR_F16) return GDR_ERR_DTYPE;
@@ -1796,13 +1899,15 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     auto encode = encode_fn();
     if (!encode) return GDR_ERR_CUDA;
 
+    // fp32 keys run their own kernel mode.
+    const int kmode = (mode == kModeFused && in_dtype == GDR_F32) ? kModeF32Keys : mode;
     // Input tiles: 64 rows x 128 bytes per box (64 bf16/fp16 key columns, or 32
-    // fp32 columns of A), 128-byte swizzle.
+    // fp32 columns of keys or of A), 128-byte swizzle.
     CUtensorMap tmap;
     {
-        const int esz = mode == kModeSolve ? 4 : 2;
+        const int esz = in_dtype == GDR_F32 ? 4 : 2;
         const int64_t cols = mode == kModeSolve ? 64 : K;
-        const CUtensorMapDataType dt = mode == kModeSolve   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+        const CUtensorMapDataType dt = in_dtype == GDR_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                        : in_dtype == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(H),
@@ -1837,7 +1942,7 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     prm.g = mode == kModeSolve ? nullptr : g;
     prm.beta = mode == kModeSolve ? nullptr : beta;
     prm.beta_kind = prm.beta ? beta_dtype : GDR_F32;
-    prm.idesc = idesc_f16_kind(in_dtype == GDR_BF16);
+    prm.idesc = kmode == kModeF32Keys ? kIdescTf32 : idesc_f16_kind(in_dtype == GDR_BF16);
     prm.cu = cu_seqlens;
     prm.out = out;
     prm.B = B;
@@ -1872,7 +1977,8 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
         if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
         return GDR_OK;
     }
-    kernel_for(mode, out_kind, static_cast<int>(K / 64))<<<gx, kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
+    const int nkb = static_cast<int>(kmode == kModeF32Keys ? K / 32 : K / 64);
+    kernel_for(kmode, out_kind, nkb)<<<gx, kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }

@@ -82,10 +82,19 @@ def _call_ex(**kw):
                                 a["H"], a["K"], a["chunk"], a["dtype"], a["out"], 0)
 
 
-@pytest.mark.parametrize("kw", [dict(kd=gdr.GDR_F32), dict(kd=3), dict(kd=-1), dict(bd=3),
-                                dict(bd=-1), dict(dtype=3)])
+@pytest.mark.parametrize("kw", [dict(kd=3), dict(kd=-1), dict(bd=3), dict(bd=-1), dict(dtype=3)])
 def test_ex_bad_dtypes(kw):
     assert _call_ex(**kw) == gdr.GDR_ERR_DTYPE
+
+
+def test_ex_fp32_key_limits():
+    import torch
+    assert _call_ex(kd=gdr.GDR_F32, K=192) == gdr.GDR_ERR_SHAPE       # fp32 keys: K <= 128
+    assert _call_ex(kd=gdr.GDR_F32, chunk=128) == gdr.GDR_ERR_DTYPE  # and chunk 64 only
+    assert _call_kkt(kd=gdr.GDR_F32) == gdr.GDR_ERR_DTYPE            # the chain takes 16-bit keys
+    if not torch.cuda.is_available():
+        assert _call_ex(kd=gdr.GDR_F32) == gdr.GDR_ERR_DEVICE
+        assert _call_ex(kd=gdr.GDR_F32, K=64) == gdr.GDR_ERR_DEVICE
 
 
 def test_ex_beta_dtype_ignored_without_beta():

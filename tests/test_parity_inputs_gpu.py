@@ -113,3 +113,20 @@ def test_fp16_all_inputs_fp16_output_large_k():
     wl = workloads.Workload("all_f16_K256", 1, 1000, 6, 256, "f16", seed=400, k_dtype="f16",
                             beta_dtype="f16")
     _parity(wl, "f16")
+
+
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("layout,out_name", [("fixed", "f32"), ("varlen", "f32"), ("fixed", "bf16")])
+def test_fp32_keys(K, layout, out_name):
+    # fp32 keys: the Gram is formed from tf32 parts and remainders (three tf32
+    # products), so fp32 output still meets the fp32 tolerance.
+    if layout == "fixed":
+        wl = workloads.Workload(f"f32keys_K{K}", 2, 300, 5, K, out_name, seed=800 + K, k_dtype="f32")
+    else:
+        wl = workloads.Workload(f"f32keys_K{K}_varlen", len(VARLEN_LENS), sum(VARLEN_LENS), 3, K, out_name,
+                                seed=810 + K, varlen_lengths=VARLEN_LENS, k_dtype="f32", beta_dtype="f32")
+    _parity(wl, out_name)
+
+
+def test_fp32_keys_many_pairs_per_cta():
+    _parity(workloads.Workload("f32keys_large", 2, 4096, 16, 128, "f32", seed=820, k_dtype="f32"), "f32")
