@@ -56,6 +56,9 @@ constexpr int kNumConsumerWarps = 4 * kNumWG;
 constexpr int kProducerWarp = kNumConsumerWarps;
 constexpr int kMmaWarp = kNumConsumerWarps + 1;
 constexpr int kNumThreads = (kNumConsumerWarps + 2) * 32;
+// The fp32-key instantiation adds two warps that split the key units.
+constexpr int kCvtWarp0 = kNumConsumerWarps + 2;
+constexpr int kNumThreadsF32Keys = kNumThreads + 64;
 
 constexpr int kBoxBytes = kChunk * 64 * 2;          // one (tile, K-half) box: 64 rows x 128 B
 constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][128 B] = 32 KB
@@ -72,7 +75,7 @@ constexpr int kOffK = 0;
 constexpr int kOffA = kOffK + kNumStages * kStageBytes;
 constexpr int kOffG = kOffA + kNumWG * kAWGBytes;
 constexpr int kOffBar = kOffG + kNumWG * kGWGBytes;
-constexpr int kNumBars = 2 * kNumStages + 2 * kNumWG;
+constexpr int kNumBars = 3 * kNumStages + 2 * kNumWG;   // full, empty, converted; tfull, tempty
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 64;
 constexpr int kSmemBytes = kSmemUsed + 1024;        // slack for 1024-byte alignment
@@ -723,7 +726,7 @@ constexpr int kModeF32Keys = 3;
 // solve mode the producer loads A tiles (two 32-column fp32 boxes per tile,
 // NKB = 2) and the MMA warp has nothing to do.
 template <int OUT, int NKB, int MODE>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 1)
     kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_out, const Params p) {
     static_assert(MODE != kModeKkt || OUT == kOutF32, "A is written as fp32");
@@ -740,6 +743,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t bar_empty = bar_full + 8 * kNumStages;            // [kNumStages]
     const uint32_t bar_tfull = bar_empty + 8 * kNumStages;           // [kNumWG]
     const uint32_t bar_tempty = bar_tfull + 8 * kNumWG;              // [kNumWG]
+    const uint32_t bar_cvt = bar_tempty + 8 * kNumWG;                // [kNumStages], fp32 keys
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     volatile int *wg_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);   // [kNumWG]
@@ -758,6 +762,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(bar_tfull + 8 * w, 1);
             mbar_init(bar_tempty + 8 * w, 4);
         }
+        for (int st = 0; st < kNumStages; ++st) mbar_init(bar_cvt + 8 * st, 2);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -850,51 +855,64 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             }
         }
-    } else if (kF32Keys && warp == kMmaWarp) {
-        // The whole warp splits each unit; lane 0 waits and issues the MMAs.
-        int64_t q = 0;
-        bool failed = false;
-        for (; q < n_local; ++q) {
+    } else if (kF32Keys && warp >= kCvtWarp0) {
+        // Converter warp c splits tile c's box of every unit in place: the tf32
+        // part (13 low mantissa bits cleared) stays, the remainder goes to the
+        // stage's second half; then it signals the unit's converted barrier.
+        const int c = warp - kCvtWarp0;
+        const int64_t units = n_local * nkc;
+        for (int64_t v = 0; v < units; ++v) {
             if (*abort_flag) break;
-            const int w = static_cast<int>(q % kNumWG);
-            const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
-            const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w);
-            for (int kc = 0; kc < nkc; ++kc) {
-                const int64_t v = q * nkc + kc;
-                const int s = static_cast<int>(v % kNumStages);
-                const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
-                int ok = 1;
-                if (lane == 0)
-                    ok = (mbar_wait(bar_full + 8 * s, ph) &&
-                          (kc != 0 || mbar_wait(bar_tempty + 8 * w, phw ^ 1))) ? 1 : 0;
-                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
-                    if (lane == 0) record_timeout(p, abort_flag);
-                    failed = true;
-                    break;
-                }
-                // Split the unit's two 64 x 32 fp32 boxes (16 KB) in place; the
-                // small parts go to the stage's second half.
-                float4 *const big = reinterpret_cast<float4 *>(smem + kOffK + s * kStageBytes);
-                float4 *const small = big + 2 * kBoxBytes / 16;
+            const int s = static_cast<int>(v % kNumStages);
+            const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(bar_full + 8 * s, ph) ? 1 : 0;
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+                if (lane == 0) record_timeout(p, abort_flag);
+                break;
+            }
+            float4 *const big = reinterpret_cast<float4 *>(smem + kOffK + s * kStageBytes + c * kBoxBytes);
+            float4 *const small = big + 2 * kBoxBytes / 16;
 #pragma unroll 4
-                for (int it = 0; it < 2 * kBoxBytes / 16 / 32; ++it) {
-                    const int idx = lane + 32 * it;
-                    const float4 x = big[idx];
-                    float4 b, m;
-                    b.x = __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
-                    b.y = __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
-                    b.z = __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
-                    b.w = __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
-                    m.x = x.x - b.x;
-                    m.y = x.y - b.y;
-                    m.z = x.z - b.z;
-                    m.w = x.w - b.w;
-                    big[idx] = b;
-                    small[idx] = m;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
+            for (int it = 0; it < kBoxBytes / 16 / 32; ++it) {
+                const int idx = lane + 32 * it;
+                const float4 x = big[idx];
+                float4 bg, m;
+                bg.x = __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+                bg.y = __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+                bg.z = __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+                bg.w = __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+                m.x = x.x - bg.x;
+                m.y = x.y - bg.y;
+                m.z = x.z - bg.z;
+                m.w = x.w - bg.w;
+                big[idx] = bg;
+                small[idx] = m;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_cvt + 8 * s);
+        }
+    } else if (kF32Keys && warp == kMmaWarp) {
+        // Lane 0 waits for the converted unit and issues the three tf32 products.
+        if (lane == 0) {
+            int64_t q = 0;
+            bool failed = false;
+            for (; q < n_local; ++q) {
+                if (*abort_flag) break;
+                const int w = static_cast<int>(q % kNumWG);
+                const uint32_t phw = static_cast<uint32_t>((q / kNumWG) & 1);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(128 * w);
+                for (int kc = 0; kc < nkc; ++kc) {
+                    const int64_t v = q * nkc + kc;
+                    const int s = static_cast<int>(v % kNumStages);
+                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                    if (!mbar_wait(bar_cvt + 8 * s, ph) ||
+                        (kc == 0 && !mbar_wait(bar_tempty + 8 * w, phw ^ 1))) {
+                        record_timeout(p, abort_flag);
+                        failed = true;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t st = sbase + kOffK + s * kStageBytes;
                     const uint32_t sm = st + 2 * kBoxBytes;
@@ -908,15 +926,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     tc_commit(bar_empty + 8 * s);
                     if (kc == nkc - 1) tc_commit(bar_tfull + 8 * w);
                 }
-                __syncwarp();
+                if (failed) break;
             }
-            if (failed) break;
-        }
-        if (lane == 0 && q > 0) {
-            const int64_t r = q - 1;
-            const int w = static_cast<int>(r % kNumWG);
-            if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
-                record_timeout(p, abort_flag);
+            if (q > 0) {
+                const int64_t r = q - 1;
+                const int w = static_cast<int>(r % kNumWG);
+                if (!mbar_wait(bar_tfull + 8 * w, static_cast<uint32_t>((r / kNumWG) & 1)))
+                    record_timeout(p, abort_flag);
+            }
         }
     } else if (warp == kMmaWarp) {
         if (kUseTmem && lane == 0) {
@@ -1978,7 +1995,8 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
         return GDR_OK;
     }
     const int nkb = static_cast<int>(kmode == kModeF32Keys ? K / 32 : K / 64);
-    kernel_for(kmode, out_kind, nkb)<<<gx, kNumThreads, kSmemBytes, st>>>(tmap, tmap_o, prm);
+    kernel_for(kmode, out_kind, nkb)<<<gx, kmode == kModeF32Keys ? kNumThreadsF32Keys : kNumThreads,
+                                        kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }
