@@ -34,7 +34,7 @@ GDR_F16 = 2
 
 EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_kkt_solve_ex", "gdr_chunk_scaled_dot_kkt",
                     "gdr_solve_tril", "gdr_kkt_solve_unfused_noalloc", "gdr_status_string",
-                    "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms")
+                    "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms", "gdr_selftest_bounded_wait")
 
 _lib = None
 _lock = threading.Lock()
@@ -79,6 +79,8 @@ def load_library():
             lib.gdr_status_string.restype = ctypes.c_char_p
             lib.gdr_kkt_solve_device_status.argtypes = [ctypes.POINTER(ci)]
             lib.gdr_kkt_solve_device_status.restype = ci
+            lib.gdr_selftest_bounded_wait.argtypes = [vp]
+            lib.gdr_selftest_bounded_wait.restype = ci
             lib.gdr_kkt_solve_num_sms.argtypes = []
             lib.gdr_kkt_solve_num_sms.restype = ci
             _lib = lib
@@ -151,6 +153,11 @@ def device_status() -> int:
     if rc != GDR_OK:
         raise GdrError(rc, "gdr_kkt_solve_device_status")
     return v.value
+
+
+def selftest_bounded_wait(stream: int = 0) -> int:
+    """Enqueues the bounded-wait self-test kernel (see the C header); returns the status."""
+    return load_library().gdr_selftest_bounded_wait(stream or None)
 
 
 def num_sms() -> int:

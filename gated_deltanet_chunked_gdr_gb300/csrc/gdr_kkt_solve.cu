@@ -165,14 +165,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits for the phase with the given parity to complete; false after kWaitNs.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false after LIMIT ns.
+template <uint64_t LIMIT>
+__device__ __noinline__ bool mbar_wait_limited(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer() - t0 > kWaitNs) return false;
+        if (global_timer() - t0 > LIMIT) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_wait_limited<kWaitNs>(bar, parity);
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int x, int y, int z) {
@@ -1702,6 +1706,22 @@ __global__ void __launch_bounds__(kC128Threads, 1)
     }
 }
 
+// ------------------------------------------------------------ wait self-test
+// One thread waits, through the kernels' bounded wait with a 20 ms limit, on a
+// barrier phase that nothing completes; when the wait runs out it records
+// GDR_ERR_TIMEOUT in the status word, as a pipeline wait of the kernels would.
+constexpr uint64_t kProbeWaitNs = 20000000ull;
+
+__global__ void bounded_wait_probe_kernel(int *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = smem_u32(&bar);
+        mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait_limited<kProbeWaitNs>(b, 0)) atomicExch(status, static_cast<int>(GDR_ERR_TIMEOUT));
+    }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
@@ -2071,6 +2091,21 @@ int gdr_kkt_solve_device_status(int *status) {
         return GDR_ERR_CUDA;
     }
     *status = v;
+    return GDR_OK;
+}
+
+int gdr_selftest_bounded_wait(void *stream) {
+    using namespace gdr;
+    int sms = 0;
+    int rc = prepare_device(&sms);
+    if (rc != GDR_OK) return rc;
+    int *status_ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status_ptr), g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        return GDR_ERR_CUDA;
+    }
+    bounded_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status_ptr);
+    if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }
 

@@ -180,6 +180,17 @@ const char *gdr_status_string(int status);
 int gdr_kkt_solve_device_status(int *status);
 
 /*
+ * gdr_selftest_bounded_wait - test hook for the failure path above (no
+ * counterpart on the pages).  Enqueues a one-thread kernel on `stream` that
+ * waits, through the kernels' own bounded wait but with a 20 ms limit, on a
+ * barrier phase that nothing completes; the wait runs out and the kernel
+ * records GDR_ERR_TIMEOUT in the device status word and returns normally, so
+ * the context stays usable.  A following gdr_kkt_solve_device_status reports
+ * GDR_ERR_TIMEOUT.  Returns GDR_OK when enqueued.
+ */
+int gdr_selftest_bounded_wait(void *stream);
+
+/*
  * gdr_kkt_solve_num_sms - number of persistent CTAs one call launches at most
  * on the current device (one per SM).  Returns a negative gdr_status on error.
  */
