@@ -1601,41 +1601,60 @@ __global__ void __launch_bounds__(kC128Threads, 1)
             }
             named_bar_sync(bar_id, 128);                       // X11, X22 complete
 
-            // ---- X21 = -X22 (A21 X11), warp -> block column J, transposed as in
-            //      the merge: P_MJ^T = sum_{K>=J} X11_KJ^T A21_MK^T, then
-            //      X21_IJ^T = -sum_{M<=I} P_MJ^T X22_IM^T.
+            // ---- X21 = -X22 (A21 X11) in two balanced rounds, transposed as in the
+            //      merge.  Round 1, warp -> block row M: P_MJ^T = sum_{K>=J}
+            //      X11_KJ^T A21_MK^T for J = 0..3 (10 products), written as P_MJ
+            //      over the warp's own A21 row of blocks.  Round 2, warp -> block
+            //      column J: X21_IJ^T = -sum_{M<=I} P_MJ^T X22_IM^T (10 products).
             {
-                const int J = qd;
+                const int M = qd;
                 float pt[4][2][4];
 #pragma unroll
-                for (int M = 0; M < 4; ++M) {
+                for (int J = 0; J < 4; ++J) {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) pt[M][nt][e] = 0.0f;
-                    for (int K2 = J; K2 < 4; ++K2) {
-                        Frag16 f;
-                        frag_from_dT<SPLIT>(blk(M0, K2, J), g8, t4, f);
-                        mma3_times_blockT<SPLIT>(pt[M], f, blk(M2, M, K2), g8, t4);
+                        for (int e = 0; e < 4; ++e) pt[J][nt][e] = 0.0f;
+#pragma unroll
+                    for (int K2 = 0; K2 < 4; ++K2) {
+                        if (K2 >= J) {
+                            Frag16 f;
+                            frag_from_dT<SPLIT>(blk(M0, K2, J), g8, t4, f);
+                            mma3_times_blockT<SPLIT>(pt[J], f, blk(M2, M, K2), g8, t4);
+                        }
                     }
                 }
-                named_bar_sync(bar_id, 128);                   // A21 no longer read
+                __syncwarp();
+#pragma unroll
+                for (int J = 0; J < 4; ++J) store_block_T(M2, M, J, pt[J], g8, t4);
+            }
+            named_bar_sync(bar_id, 128);                       // P complete
+            {
+                const int J = qd;
+                float xt[4][2][4];
 #pragma unroll
                 for (int I = 0; I < 4; ++I) {
-                    float acc[2][4] = {};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) xt[I][nt][e] = 0.0f;
 #pragma unroll
                     for (int M = 0; M < 4; ++M) {
                         if (M <= I) {
                             Frag16 f;
-                            frag_from_acc<SPLIT>(pt[M], f);
-                            mma3_times_blockT<SPLIT>(acc, f, blk(M1, I, M), g8, t4);
+                            frag_from_dT<SPLIT>(blk(M2, M, J), g8, t4, f);
+                            mma3_times_blockT<SPLIT>(xt[I], f, blk(M1, I, M), g8, t4);
                         }
                     }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int I = 0; I < 4; ++I) {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[nt][e] = -acc[nt][e];
-                    store_block_T(M2, I, J, acc, g8, t4);
+                        for (int e = 0; e < 4; ++e) xt[I][nt][e] = -xt[I][nt][e];
+                    store_block_T(M2, I, J, xt[I], g8, t4);
                 }
             }
             named_bar_sync(bar_id, 128);                       // X complete
