@@ -1249,25 +1249,27 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
 // columns).  With the halves' inverses X11 = (I + A11)^{-1} and
 // X22 = (I + A22)^{-1} (the 64-token solve on each half),
 //     X = [[X11, 0], [X21, X22]],   X21 = -X22 A21 X11,
-// and X21 comes from two more block products on the tensor cores.  Two
-// consumer warpgroups (128 rows each); per warpgroup three 64 x 64 fp32
-// matrices: M0 = A11 then X11, M1 = A22 then X22, M2 = A21 then X21.
-constexpr int kC128WG = 2;
+// and X21 comes from two more block products on the tensor cores.  Three
+// consumer warpgroups (128 rows each) on a two-stage key ring; per warpgroup
+// three 64 x 64 fp32 matrices: M0 = A11 then X11, M1 = A22 then X22, M2 = A21
+// then X21.
+constexpr int kC128WG = 3;
+constexpr int kC128Stages = 2;
 constexpr int kC128Producer = 4 * kC128WG;
 constexpr int kC128Mma = 4 * kC128WG + 1;
 constexpr int kC128Threads = 32 * (4 * kC128WG + 2);
 constexpr int kMatBytes = kChunk * kAPitch * 4;           // 17408
 constexpr int kC128M1Off = kMatBytes + 16;                // other banks than M0
 constexpr int kC128M2Off = 2 * kMatBytes + 32;
-constexpr int kC128WGBytes = 53248;                       // >= kC128M2Off + kMatBytes, multiple of 1024
+constexpr int kC128WGBytes = kC128M2Off + kMatBytes;       // 52256 (16-byte aligned matrices)
 constexpr int kC128GBytes = 2 * 2 * 128 * 4;              // g and v of 128 rows, double buffered
-constexpr int kC128OffA = kOffK + kNumStages * kStageBytes;
+constexpr int kC128OffA = kOffK + kC128Stages * kStageBytes;
 constexpr int kC128OffG = kC128OffA + kC128WG * kC128WGBytes;
 constexpr int kC128OffBar = kC128OffG + kC128WG * kC128GBytes;
-constexpr int kC128OffMisc = kC128OffBar + (2 * kNumStages + 2 * kC128WG) * 8;
+constexpr int kC128OffMisc = kC128OffBar + (2 * kC128Stages + 2 * kC128WG) * 8;
 constexpr int kC128SmemBytes = kC128OffMisc + 64 + 1024;
-constexpr uint32_t kC128TmemCols = 256;
-static_assert(kC128M2Off + kMatBytes <= kC128WGBytes, "chunk-128 matrices");
+constexpr uint32_t kC128TmemCols = 512;
+static_assert(kC128WGBytes % 16 == 0, "chunk-128 matrices");
 static_assert(kC128SmemBytes <= 232448, "chunk-128 shared memory budget");
 
 // The half tt (0 or 1) of a 128-token chunk as a 64-row tile.
@@ -1288,9 +1290,9 @@ __global__ void __launch_bounds__(kC128Threads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + kC128OffBar;                   // [kNumStages]
-    const uint32_t bar_empty = bar_full + 8 * kNumStages;            // [kNumStages]
-    const uint32_t bar_tfull = bar_empty + 8 * kNumStages;           // [kC128WG]
+    const uint32_t bar_full = sbase + kC128OffBar;                   // [kC128Stages]
+    const uint32_t bar_empty = bar_full + 8 * kC128Stages;            // [kC128Stages]
+    const uint32_t bar_tfull = bar_empty + 8 * kC128Stages;           // [kC128WG]
     const uint32_t bar_tempty = bar_tfull + 8 * kC128WG;             // [kC128WG]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kC128OffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kC128OffMisc + 4);
@@ -1299,7 +1301,7 @@ __global__ void __launch_bounds__(kC128Threads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kNumStages; ++s) {
+        for (int s = 0; s < kC128Stages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
@@ -1359,8 +1361,8 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                 for (kc = 0; kc < nkc; ++kc) {
                     const int64_t v = q * nkc + kc;
                     const int nb = (2 * kc + 1 < nkb) ? 2 : 1;
-                    const int s = static_cast<int>(v % kNumStages);
-                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                    const int s = static_cast<int>(v % kC128Stages);
+                    const uint32_t ph = static_cast<uint32_t>((v / kC128Stages) & 1);
                     const uint32_t st = sbase + kOffK + s * kStageBytes;
                     int ok = 1;
                     if (lane == 0) {
@@ -1382,10 +1384,10 @@ __global__ void __launch_bounds__(kC128Threads, 1)
             }
             const int64_t v = q * nkc + (failed ? kc : 0);
             if (lane == 0) {
-                const int64_t first = v > kNumStages ? v - kNumStages : 0;
+                const int64_t first = v > kC128Stages ? v - kC128Stages : 0;
                 for (int64_t r = first; r < v; ++r) {
-                    const int s = static_cast<int>(r % kNumStages);
-                    const uint32_t ph = static_cast<uint32_t>((r / kNumStages) & 1);
+                    const int s = static_cast<int>(r % kC128Stages);
+                    const uint32_t ph = static_cast<uint32_t>((r / kC128Stages) & 1);
                     if (!mbar_wait(bar_full + 8 * s, ph)) record_timeout(p, abort_flag);
                     if (!mbar_wait(bar_empty + 8 * s, ph)) record_timeout(p, abort_flag);
                 }
@@ -1403,8 +1405,8 @@ __global__ void __launch_bounds__(kC128Threads, 1)
 #pragma unroll
                 for (int kc = 0; kc < nkc; ++kc) {
                     const int64_t v = q * nkc + kc;
-                    const int s = static_cast<int>(v % kNumStages);
-                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+                    const int s = static_cast<int>(v % kC128Stages);
+                    const uint32_t ph = static_cast<uint32_t>((v / kC128Stages) & 1);
                     if (!mbar_wait(bar_full + 8 * s, ph) ||
                         (kc == 0 && !mbar_wait(bar_tempty + 8 * w, phw ^ 1))) {
                         record_timeout(p, abort_flag);
