@@ -1,6 +1,6 @@
 """Throughput benchmark of the chunk-forward kkt_solve step on GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c5]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
 
 One step = one kkt_solve over the whole workload ((2, 16384, 32, 128), bf16 keys,
 bf16 output by default) with inputs already resident in HBM.  The step's
@@ -35,7 +35,7 @@ METRIC = "token-heads/s and achieved HBM GB/s (% of GB300 peak) for kkt_solve, 1
 UNIT = "token-heads/s"
 # Ascend 910B fused time for (2,16384,32,128) from the MindSpeed-Ops PR page's
 # performance table: 4.9368 ms -> 1,048,576 token-heads / 4.9368 ms.
-PAGE_FUSED_MS = {"c5": 4.9368}
+PAGE_FUSED_MS = {"B2_T16384_H32_K128": 4.9368}
 
 
 ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4}
@@ -229,7 +229,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c5", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="B2_T16384_H32_K128", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--out-dtype", default=None, choices=["f32", "bf16", "f16"])
     ap.add_argument("--K", type=int, default=None, choices=[64, 128, 192, 256],
                     help="head dimension (default: the workload's, 128)")

@@ -16,7 +16,7 @@ sys.path.insert(0, os.path.dirname(os.path.dirname(HERE)))
 import oracle  # noqa: E402
 import workloads  # noqa: E402
 
-WL = workloads.CONFIGS["c2"].with_(name="golden_B2_T100_H5_K128", T=100)
+WL = workloads.CONFIGS["B2_T2000_H5_K128"].with_(name="golden_B2_T100_H5_K128", T=100)
 
 
 def rows_to_store(wl):

@@ -24,7 +24,7 @@ def test_bounded_wait_runs_out_reports_timeout_and_context_survives():
     assert gdr.selftest_bounded_wait() == gdr.GDR_OK
     assert gdr.device_status() == gdr.GDR_ERR_TIMEOUT   # the wait ran out and was recorded
     assert gdr.device_status() == gdr.GDR_OK            # reading resets it
-    inp = workloads.make_inputs(workloads.CONFIGS["c1"])
+    inp = workloads.make_inputs(workloads.CONFIGS["B1_T256_H8_K128"])
     out = gdr.kkt_solve(inp["k"].to(dev), inp["g"].to(dev), inp["beta"].to(dev))
     torch.cuda.synchronize(dev)
     assert gdr.device_status() == gdr.GDR_OK

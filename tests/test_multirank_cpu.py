@@ -58,7 +58,7 @@ def test_reference_arm_prints_once_under_torchrun():
     env = dict(os.environ, OMP_NUM_THREADS="1")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
-           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "c1",
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "B1_T256_H8_K128",
            "--steps", "3", "--warmup", "3", "--gpus", "2"]
     out = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert out.returncode == 0, out.stderr[-2000:]

@@ -49,7 +49,7 @@ PINS = [
     (pins.test_chunk_A_hand_values, {}),
     (pins.test_solve_tril_equals_library_inverse_and_reads_only_strict_lower, {}),
     (pins.test_solve_tril_L3_closed_form, {}),
-    (pins.test_chain_of_halves_equals_fused_oracle, dict(name="c1")),
+    (pins.test_chain_of_halves_equals_fused_oracle, dict(name="B1_T256_H8_K128")),
 ]
 
 

@@ -249,7 +249,7 @@ def test_fixed_length_batches_are_separate_sequences():
 
 
 def test_threads_do_not_change_results():
-    wl = workloads.CONFIGS["c2"].with_(T=300)
+    wl = workloads.CONFIGS["B2_T2000_H5_K128"].with_(T=300)
     inp = workloads.make_inputs(wl)
     a = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], threads=1)
     b = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], threads=5)
@@ -257,7 +257,7 @@ def test_threads_do_not_change_results():
 
 
 def test_tiles_api_matches_full_run():
-    wl = workloads.CONFIGS["c2"].with_(T=150)
+    wl = workloads.CONFIGS["B2_T2000_H5_K128"].with_(T=150)
     inp = workloads.make_inputs(wl)
     full = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], threads=2).reshape(-1, wl.H, C)
     tiles = workloads.tile_list(wl)
@@ -330,7 +330,7 @@ def test_solve_tril_L3_closed_form():
     assert np.abs(X - want).max() <= 1e-15
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "varlen"])
+@pytest.mark.parametrize("name", ["B1_T256_H8_K128", "B2_T2000_H5_K128", "varlen"])
 def test_chain_of_halves_equals_fused_oracle(name):
     if name == "varlen":
         lens = (1, 64, 0, 65, 130, 2)

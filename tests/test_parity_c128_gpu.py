@@ -97,4 +97,4 @@ def test_none_variants(use_g, use_beta):
 def test_varlen():
     lens = (1, 128, 0, 129, 64, 65, 300, 2, 255)
     _parity(_wl("c128_varlen", len(lens), sum(lens), 3, seed=716, varlen_lengths=lens), "f32")
-    _parity(workloads.CONFIGS["c4"].with_(chunk=C, name="c4_c128"), "f32")
+    _parity(workloads.CONFIGS["varlen8_H16_K128"].with_(chunk=C, name="c4_c128"), "f32")

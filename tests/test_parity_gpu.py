@@ -72,15 +72,15 @@ def _full_parity(wl, out_dtype, dev):
 
 
 @pytest.mark.parametrize("name,out_dtype", [
-    ("c1", torch.float32), ("c2", torch.float32), ("c3", torch.bfloat16), ("c3", torch.float32),
-    ("c4", torch.float32), ("c1", torch.bfloat16), ("c4", torch.bfloat16)])
+    ("B1_T256_H8_K128", torch.float32), ("B2_T2000_H5_K128", torch.float32), ("B1_T8192_H8_K128", torch.bfloat16), ("B1_T8192_H8_K128", torch.float32),
+    ("varlen8_H16_K128", torch.float32), ("B1_T256_H8_K128", torch.bfloat16), ("varlen8_H16_K128", torch.bfloat16)])
 def test_workload_full_parity(name, out_dtype):
     _full_parity(workloads.CONFIGS[name], out_dtype, _dev())
 
 
 @pytest.mark.parametrize("use_g,use_beta", [(False, True), (True, False), (False, False)])
 def test_none_variants_partial_chunk_odd_heads(use_g, use_beta):
-    wl = workloads.CONFIGS["c2"].with_(use_g=use_g, use_beta=use_beta)
+    wl = workloads.CONFIGS["B2_T2000_H5_K128"].with_(use_g=use_g, use_beta=use_beta)
     _full_parity(wl, torch.float32, _dev())
 
 
@@ -100,7 +100,7 @@ def test_varlen_edge_lengths_and_empty_sequence():
 
 def test_varlen_equals_separate_runs():
     dev = _dev()
-    wl = workloads.CONFIGS["c4"]
+    wl = workloads.CONFIGS["varlen8_H16_K128"]
     inp = workloads.make_inputs(wl)
     packed = _run(inp, torch.float32, dev)
     cu = workloads.cu_seqlens_of(wl)
@@ -115,7 +115,7 @@ def test_varlen_equals_separate_runs():
 def test_steep_gate_within_clamp():
     # log-gates falling by up to ~0.7 per token: differences down to about -44.
     dev = _dev()
-    wl = workloads.CONFIGS["c1"]
+    wl = workloads.CONFIGS["B1_T256_H8_K128"]
     inp = workloads.make_inputs(wl)
     rng = np.random.default_rng(9)
     a = -0.7 * rng.random((wl.B * wl.T, wl.H)).astype(np.float32)
@@ -146,7 +146,7 @@ def test_gate_range_beyond_factorisation_guard(out_dtype):
     # Decays up to 3 per token: a chunk's log-gate spans ~95, beyond the range
     # where exp(g_i - g_j) is factored, so the direct clamped form runs.
     dev = _dev()
-    wl = workloads.CONFIGS["c2"]
+    wl = workloads.CONFIGS["B2_T2000_H5_K128"]
     inp = _with_gate(wl, lambda rng, sh: -3.0 * rng.random(sh), 31)
     out = _run(inp, out_dtype, dev)
     ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"])
@@ -156,7 +156,7 @@ def test_gate_range_beyond_factorisation_guard(out_dtype):
 def test_non_monotone_gate():
     # Log-gates that rise and fall inside a chunk (|steps| <= 0.3).
     dev = _dev()
-    wl = workloads.CONFIGS["c1"]
+    wl = workloads.CONFIGS["B1_T256_H8_K128"]
     inp = _with_gate(wl, lambda rng, sh: rng.uniform(-0.3, 0.3, sh), 32)
     out = _run(inp, torch.float32, dev)
     ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"])
@@ -169,7 +169,7 @@ def test_bf16_output_against_fp32_output():
     # within bf16 rounding plus a tf32-level term, and the unit diagonal and
     # the zero upper triangle must be exact.
     dev = _dev()
-    inp = workloads.make_inputs(workloads.CONFIGS["c2"])
+    inp = workloads.make_inputs(workloads.CONFIGS["B2_T2000_H5_K128"])
     f32 = _run(inp, torch.float32, dev).double()
     bf = _run(inp, torch.bfloat16, dev).double()
     diff = (bf - f32).abs()
@@ -185,7 +185,7 @@ def test_bf16_output_against_fp32_output():
 
 def test_deterministic_and_stream_aware():
     dev = _dev()
-    inp = workloads.make_inputs(workloads.CONFIGS["c4"])
+    inp = workloads.make_inputs(workloads.CONFIGS["varlen8_H16_K128"])
     a = _run(inp, torch.float32, dev)
     s = torch.cuda.Stream(dev)
     with torch.cuda.stream(s):
@@ -237,7 +237,7 @@ def test_golden_fixture_rows():
 
 def test_full_size_bf16_sampled_parity_and_invariants():
     dev = _dev()
-    wl = workloads.CONFIGS["c5"]
+    wl = workloads.CONFIGS["B2_T16384_H32_K128"]
     inp = workloads.make_inputs(wl)
     out = _run(inp, torch.bfloat16, dev)
     flat = out.view(-1, wl.H, 64)
@@ -253,4 +253,4 @@ def test_full_size_bf16_sampled_parity_and_invariants():
     tiles = workloads.sample_tiles(wl, 256)
     refs = oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], tiles)
     got = np.concatenate([flat[r0:r0 + L, h].double().cpu().numpy() for (_, _, h, r0, L) in tiles])
-    _check(got, np.concatenate(refs), torch.bfloat16, "c5 sampled")
+    _check(got, np.concatenate(refs), torch.bfloat16, "B2_T16384_H32_K128 sampled")

@@ -91,7 +91,7 @@ def test_head_dims_many_pairs_per_cta(K):
     _parity(wl, "f32")
 
 
-@pytest.mark.parametrize("name", ["c2", "c4"])
+@pytest.mark.parametrize("name", ["B2_T2000_H5_K128", "varlen8_H16_K128"])
 def test_fp16_keys(name):
     wl = workloads.CONFIGS[name].with_(k_dtype="f16")
     _parity(wl, "f32")
@@ -100,11 +100,11 @@ def test_fp16_keys(name):
 @pytest.mark.parametrize("beta_dtype", ["f32", "f16"])
 @pytest.mark.parametrize("k_dtype", ["bf16", "f16"])
 def test_beta_dtypes(beta_dtype, k_dtype):
-    wl = workloads.CONFIGS["c2"].with_(beta_dtype=beta_dtype, k_dtype=k_dtype)
+    wl = workloads.CONFIGS["B2_T2000_H5_K128"].with_(beta_dtype=beta_dtype, k_dtype=k_dtype)
     _parity(wl, "f32")
 
 
-@pytest.mark.parametrize("name", ["c2", "c3", "c4"])
+@pytest.mark.parametrize("name", ["B2_T2000_H5_K128", "B1_T8192_H8_K128", "varlen8_H16_K128"])
 def test_fp16_output(name):
     _parity(workloads.CONFIGS[name], "f16")
 

@@ -50,11 +50,11 @@ def _workload(name):
     if name == "K256":
         return workloads.Workload("chain_K256", 2, 300, 5, 256, "f32", seed=502)
     if name == "c2_nog":
-        return workloads.CONFIGS["c2"].with_(use_g=False)
+        return workloads.CONFIGS["B2_T2000_H5_K128"].with_(use_g=False)
     return workloads.CONFIGS[name]
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c2_nog", "c4", "varlen", "K256"])
+@pytest.mark.parametrize("name", ["B1_T256_H8_K128", "B2_T2000_H5_K128", "c2_nog", "varlen8_H16_K128", "varlen", "K256"])
 def test_A_against_oracle(name):
     dev = _dev()
     wl = _workload(name)
@@ -113,8 +113,8 @@ def test_solve_tril_of_given_A(layout, out_name):
         assert np.all(d <= np.abs(ref) * 2.0 ** -10 + 2e-5)
 
 
-@pytest.mark.parametrize("name,out_name", [("c1", "f32"), ("c2", "f32"), ("c2_nog", "f32"),
-                                           ("c3", "bf16"), ("c3", "f32"), ("c4", "f32"),
+@pytest.mark.parametrize("name,out_name", [("B1_T256_H8_K128", "f32"), ("B2_T2000_H5_K128", "f32"), ("c2_nog", "f32"),
+                                           ("B1_T8192_H8_K128", "bf16"), ("B1_T8192_H8_K128", "f32"), ("varlen8_H16_K128", "f32"),
                                            ("varlen", "bf16"), ("K256", "f16")])
 def test_chain_equals_fused_bit_for_bit(name, out_name):
     dev = _dev()

@@ -54,7 +54,7 @@ def test_noalloc_matches_the_existing_entry_point_on_two_calls_in_a_row():
     stream = torch.cuda.current_stream(dev).cuda_stream
     lens = (1, 64, 0, 65, 130, 2, 200, 63)
     calls = [
-        (workloads.CONFIGS["c4"], torch.float32),                       # varlen, 262144 token-heads at most
+        (workloads.CONFIGS["varlen8_H16_K128"], torch.float32),                       # varlen, 262144 token-heads at most
         (workloads.Workload("noalloc_small", 2, 300, 5, 128, "bf16", seed=601), torch.bfloat16),
         (workloads.Workload("noalloc_varlen", len(lens), sum(lens), 3, 256, "f32", seed=602,
                             varlen_lengths=lens), torch.float32),

@@ -70,13 +70,13 @@ def varlen_workload(name: str, seed: int, H: int = 16, K: int = 128, out_dtype: 
                     seed=seed, varlen_lengths=lens)
 
 
-# The five workloads.  Seed = workload number.
+# The workloads, named by their shapes; seeds 1 to 5.
 CONFIGS = {
-    "c1": Workload("c1_B1_T256_H8_K128", 1, 256, 8, 128, "f32", seed=1),
-    "c2": Workload("c2_B2_T2000_H5_K128", 2, 2000, 5, 128, "f32", seed=2),
-    "c3": Workload("c3_B1_T8192_H8_K128", 1, 8192, 8, 128, "bf16", seed=3),
-    "c4": varlen_workload("c4_varlen8_H16_K128", seed=4),
-    "c5": Workload("c5_B2_T16384_H32_K128", 2, 16384, 32, 128, "bf16", seed=5),
+    "B1_T256_H8_K128": Workload("B1_T256_H8_K128", 1, 256, 8, 128, "f32", seed=1),
+    "B2_T2000_H5_K128": Workload("B2_T2000_H5_K128", 2, 2000, 5, 128, "f32", seed=2),
+    "B1_T8192_H8_K128": Workload("B1_T8192_H8_K128", 1, 8192, 8, 128, "bf16", seed=3),
+    "varlen8_H16_K128": varlen_workload("varlen8_H16_K128", seed=4),
+    "B2_T16384_H32_K128": Workload("B2_T16384_H32_K128", 2, 16384, 32, 128, "bf16", seed=5),
 }
 
 
