@@ -254,3 +254,39 @@ def test_full_size_bf16_sampled_parity_and_invariants():
     refs = oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], tiles)
     got = np.concatenate([flat[r0:r0 + L, h].double().cpu().numpy() for (_, _, h, r0, L) in tiles])
     _check(got, np.concatenate(refs), torch.bfloat16, "B2_T16384_H32_K128 sampled")
+
+
+def _sampled_parity_and_invariants(wl, out_dtype, count):
+    dev = _dev()
+    inp = workloads.make_inputs(wl)
+    out = _run(inp, out_dtype, dev)
+    flat = out.view(-1, wl.H, 64)
+    rows = torch.from_numpy(_real_rows(wl)).to(dev)
+    real = flat.index_select(0, rows)
+    assert torch.isfinite(real).all()
+    loc = torch.from_numpy(np.concatenate([np.arange(e - s) % 64 for s, e in workloads._sequence_bounds(wl)])).to(dev)
+    diag = real.gather(2, loc.view(-1, 1, 1).expand(-1, wl.H, 1)).squeeze(-1)
+    assert torch.all(diag == 1)
+    upper = torch.arange(64, device=dev).view(1, 1, 64) > loc.view(-1, 1, 1)
+    assert torch.all(real.masked_select(upper) == 0)
+    tiles = workloads.sample_tiles(wl, count)
+    refs = oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], tiles)
+    got = np.concatenate([flat[r0:r0 + L, h].double().cpu().numpy() for (_, _, h, r0, L) in tiles])
+    _check(got, np.concatenate(refs), out_dtype, wl.name)
+
+
+def test_long_walks_many_pairs_per_cta():
+    # 2^21 tokens of one head: every CTA walks over a hundred pairs, and the
+    # chunk index crosses NT many times per warpgroup stride.
+    wl = workloads.Workload("B1_T2097152_H1_K128", 1, 1 << 21, 1, 128, "f32", seed=901)
+    _sampled_parity_and_invariants(wl, torch.float32, 512)
+
+
+def test_thousands_of_packed_sequences():
+    # 4000 packed sequences of 0..300 tokens (many empty, many shorter than a
+    # chunk): the schedule steps over sequence boundaries at almost every pair.
+    rng = np.random.default_rng(902)
+    lens = tuple(int(x) for x in np.where(rng.random(4000) < 0.15, 0, rng.integers(1, 301, size=4000)))
+    wl = workloads.Workload("varlen4000_H3_K128", len(lens), sum(lens), 3, 128, "bf16", seed=903,
+                            varlen_lengths=lens)
+    _sampled_parity_and_invariants(wl, torch.bfloat16, 1024)
