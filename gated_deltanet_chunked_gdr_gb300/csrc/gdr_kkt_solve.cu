@@ -1506,52 +1506,44 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                 const int npass = hf ? 2 : 1;
                 for (int pass = 0; pass < npass; ++pass) {
                     const int cb = pass == 0 ? 64 * hf : 0;        // TMEM columns = partner rows
-                    uint32_t sr[64];
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
-                                           static_cast<uint32_t>(128 * wg + cb);
-                    {
-                        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
-                        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
-                        tmem_ld32(taddr, lo);
-                        tmem_ld32(taddr + 32, hi);
-                    }
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) reg_fence(sr[j]);
-                    float4 *Arow = reinterpret_cast<float4 *>((pass == 0 ? Mh(hf) : M2) + ih * kAPitch);
+                    float *const Arowf = (pass == 0 ? Mh(hf) : M2) + ih * kAPitch;
                     // Diagonal block rows 0..31 only need columns j < 32.
-                    const int n4 = (pass == 1 || (qd & 1)) ? 16 : 8;
-                    const float4 *vj = reinterpret_cast<const float4 *>(vcur + cb);
-                    const float4 *gj = reinterpret_cast<const float4 *>(gcur + cb);
-                    if (!rowok) {
-                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int nh = (pass == 1 || (qd & 1)) ? 2 : 1;
+                    for (int hh = 0; hh < nh; ++hh) {              // 32 columns at a time
+                        uint32_t sr[32];
+                        tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * qd) << 16) +
+                                      static_cast<uint32_t>(128 * wg + cb + 32 * hh),
+                                  sr);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int j4 = 0; j4 < 16; ++j4)
-                            if (j4 < n4) Arow[j4] = z;
-                    } else if (!direct) {
+                        for (int j = 0; j < 32; ++j) reg_fence(sr[j]);
+                        float4 *Arow = reinterpret_cast<float4 *>(Arowf + 32 * hh);
+                        const float4 *vj = reinterpret_cast<const float4 *>(vcur + cb + 32 * hh);
+                        const float4 *gj = reinterpret_cast<const float4 *>(gcur + cb + 32 * hh);
+                        if (!rowok) {
 #pragma unroll
-                        for (int j4 = 0; j4 < 16; ++j4) {
-                            if (j4 < n4) {
+                            for (int j4 = 0; j4 < 8; ++j4) Arow[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        } else if (!direct) {
+#pragma unroll
+                            for (int j4 = 0; j4 < 8; ++j4) {
                                 const float4 v = vj[j4];
-                                float4 a;
-                                a.x = (__uint_as_float(sr[4 * j4 + 0]) * w) * v.x;
-                                a.y = (__uint_as_float(sr[4 * j4 + 1]) * w) * v.y;
-                                a.z = (__uint_as_float(sr[4 * j4 + 2]) * w) * v.z;
-                                a.w = (__uint_as_float(sr[4 * j4 + 3]) * w) * v.w;
-                                Arow[j4] = a;
+                                float4 x;
+                                x.x = (__uint_as_float(sr[4 * j4 + 0]) * w) * v.x;
+                                x.y = (__uint_as_float(sr[4 * j4 + 1]) * w) * v.y;
+                                x.z = (__uint_as_float(sr[4 * j4 + 2]) * w) * v.z;
+                                x.w = (__uint_as_float(sr[4 * j4 + 3]) * w) * v.w;
+                                Arow[j4] = x;
                             }
-                        }
-                    } else {
+                        } else {
 #pragma unroll
-                        for (int j4 = 0; j4 < 16; ++j4) {
-                            if (j4 < n4) {
+                            for (int j4 = 0; j4 < 8; ++j4) {
                                 const float4 gg = gj[j4];
-                                float4 a;
-                                a.x = bi * __uint_as_float(sr[4 * j4 + 0]) * __expf(fminf(fmaxf(gi - gg.x, -50.f), 50.f));
-                                a.y = bi * __uint_as_float(sr[4 * j4 + 1]) * __expf(fminf(fmaxf(gi - gg.y, -50.f), 50.f));
-                                a.z = bi * __uint_as_float(sr[4 * j4 + 2]) * __expf(fminf(fmaxf(gi - gg.z, -50.f), 50.f));
-                                a.w = bi * __uint_as_float(sr[4 * j4 + 3]) * __expf(fminf(fmaxf(gi - gg.w, -50.f), 50.f));
-                                Arow[j4] = a;
+                                float4 x;
+                                x.x = bi * __uint_as_float(sr[4 * j4 + 0]) * __expf(fminf(fmaxf(gi - gg.x, -50.f), 50.f));
+                                x.y = bi * __uint_as_float(sr[4 * j4 + 1]) * __expf(fminf(fmaxf(gi - gg.y, -50.f), 50.f));
+                                x.z = bi * __uint_as_float(sr[4 * j4 + 2]) * __expf(fminf(fmaxf(gi - gg.z, -50.f), 50.f));
+                                x.w = bi * __uint_as_float(sr[4 * j4 + 3]) * __expf(fminf(fmaxf(gi - gg.w, -50.f), 50.f));
+                                Arow[j4] = x;
                             }
                         }
                     }
