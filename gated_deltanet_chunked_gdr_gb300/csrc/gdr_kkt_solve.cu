@@ -31,6 +31,12 @@
 //                  store    - X is assembled in a 128-byte-swizzled staging copy
 //                             and written by TMA (full chunks) or by 128-bit
 //                             stores (a chunk cut short by the sequence end).
+// The same template also builds: fp16 keys and K = 64..256 (the key type only
+// changes the TMA map and the MMA descriptor; K / 64 sets the stage units per
+// pair); fp32 keys (two more warps split each unit into tf32 parts for a
+// three-product tf32 Gram); the two halves of the page's unfused chain (A
+// written to HBM; the solve of a given A).  kkt_solve_c128_kernel handles
+// 128-token chunks.
 // Every mbarrier wait is bounded by wall time; on expiry the kernel records
 // GDR_ERR_TIMEOUT in a device status word and all roles leave their loops.
 
