@@ -337,6 +337,33 @@ def main():
         ms_total = sum(a.elapsed_time(b) for a, b in per_step)
     ms_total = reduce_max(ms_total, ws, dev)
     ms_step = ms_total / args.steps
+
+    # Spread of single launches (median, p10, p90), each launch between its own
+    # pair of events; a small workload reuses its cold per-step times and adds
+    # the warm mean of back-to-back launches for comparison.
+    if flush is None:
+        spread_n = min(args.steps, 500)
+        per_launch = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(spread_n)]
+        for a, b in per_launch:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+    else:
+        per_launch = per_step
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in per_launch)
+    launch_stats = {"launches": len(us), "l2": "cold" if flush is not None else "not flushed (> 2 x L2)",
+                    "median_us": statistics.median(us),
+                    "p10_us": us[int(0.1 * (len(us) - 1))], "p90_us": us[int(0.9 * (len(us) - 1))]}
+    if flush is not None:
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for _ in range(args.steps):
+            step()
+        w1.record(stream)
+        torch.cuda.synchronize(dev)
+        launch_stats["warm_mean_us"] = w0.elapsed_time(w1) * 1e3 / args.steps
     del flush
     value = aggregate_value(th_rank, ms_step, ws)
     if gdr.device_status() != gdr.GDR_OK:
@@ -445,6 +472,7 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,
+            "launch_stats": launch_stats,
             "clocks": clocks,
             "unfused_chain": None if chain_ms is None else {
                 "what": "gdr_chunk_scaled_dot_kkt then gdr_solve_tril (A fp32 through HBM), same inputs",

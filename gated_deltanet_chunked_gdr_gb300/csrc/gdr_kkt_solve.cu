@@ -33,7 +33,8 @@
 //                             stores (a chunk cut short by the sequence end).
 // The same template also builds: fp16 keys and K = 64..256 (the key type only
 // changes the TMA map and the MMA descriptor; K / 64 sets the stage units per
-// pair); fp32 keys (two more warps split each unit into tf32 parts for a
+// pair); fp32 keys (bf16 output: one tf32 product on the keys as loaded;
+// fp32 or fp16 output: two more warps split each unit into tf32 parts for a
 // three-product tf32 Gram); the two halves of the page's unfused chain (A
 // written to HBM; the solve of a given A).  kkt_solve_c128_kernel handles
 // 128-token chunks.
@@ -728,6 +729,12 @@ constexpr int kModeFused = 0, kModeKkt = 1, kModeSolve = 2;
 // small = x - big, and the Gram is big big^T + big small^T + small big^T on the
 // kind::tf32 tensor cores (the dropped small small^T is below 2^-20 relative).
 constexpr int kModeF32Keys = 3;
+// The fused step with fp32 keys and bf16 output: the key units are the boxes of
+// fp32 columns as loaded, the MMA warp issues one kind::tf32 product per K step
+// on them, and no split is made.  Narrowing an fp32 key to tf32 changes it by
+// at most 2^-10 of its value (truncated or rounded), which leaves the result
+// within a fraction of one bf16 rounding of the output.
+constexpr int kModeF32KeysTf32 = 4;
 
 // OUT: kOutF32, kOutBF16 or kOutF16.  The merge runs split (fp32-accurate) for
 // fp32 and fp16 output and as one tf32 pass for bf16 output.  NKB = K / 64, the
@@ -744,7 +751,8 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
     constexpr bool kUseTmem = MODE != kModeSolve;
     constexpr bool kF32Keys = MODE == kModeF32Keys;
     // Elements per 128-byte box row: 64 bf16/fp16 key columns, or 32 fp32 ones.
-    constexpr int kBoxCols = (MODE == kModeSolve || kF32Keys) ? 32 : 64;
+    constexpr bool kTf32Gram = MODE == kModeF32KeysTf32;
+    constexpr int kBoxCols = (MODE == kModeSolve || kF32Keys || kTf32Gram) ? 32 : 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -975,8 +983,12 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint32_t a_addr = st + kh * 2 * kBoxBytes + ks * 32;
-                            tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(a_addr), p.idesc,
-                                       (kc | kh | ks) ? 1u : 0u);
+                            if constexpr (kTf32Gram)
+                                tc_mma_tf32(d, smem_desc_sw128(a_addr), smem_desc_sw128(a_addr), p.idesc,
+                                            (kc | kh | ks) ? 1u : 0u);
+                            else
+                                tc_mma_f16(d, smem_desc_sw128(a_addr), smem_desc_sw128(a_addr), p.idesc,
+                                           (kc | kh | ks) ? 1u : 0u);
                         }
                     }
                     tc_commit(bar_empty + 8 * s);
@@ -1788,6 +1800,8 @@ KernelFn kernel_for(int mode, int out_kind, int nkb) {
         if (out_kind == kOutF16) return nkb == 2 ? kkt_solve_kernel<kOutF16, 2, kModeF32Keys> : kkt_solve_kernel<kOutF16, 4, kModeF32Keys>;
         return nkb == 2 ? kkt_solve_kernel<kOutF32, 2, kModeF32Keys> : kkt_solve_kernel<kOutF32, 4, kModeF32Keys>;
     }
+    if (mode == kModeF32KeysTf32)   // bf16 output only; nkb = K / 32: 2 or 4
+        return nkb == 2 ? kkt_solve_kernel<kOutBF16, 2, kModeF32KeysTf32> : kkt_solve_kernel<kOutBF16, 4, kModeF32KeysTf32>;
     if (out_kind == kOutBF16) return kernel_for_nkb<kOutBF16, kModeFused>(nkb);
     if (out_kind == kOutF16) return kernel_for_nkb<kOutF16, kModeFused>(nkb);
     return kernel_for_nkb<kOutF32, kModeFused>(nkb);
@@ -1860,6 +1874,10 @@ int prepare_device(int *sms) {
                 attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(kModeF32Keys, o, n),
                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                           kSmemBytes) == cudaSuccess;
+        for (int n = 2; n <= 4; n += 2)
+            attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(kModeF32KeysTf32, kOutBF16, n),
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      kSmemBytes) == cudaSuccess;
         for (int o = 0; o < 3; ++o)
             for (int n = 1; n <= 2; ++n)
                 attr_ok = attr_ok && cudaFuncSetAttribute(kernel_c128_for(o, n),
@@ -1956,7 +1974,9 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     if (!encode) return GDR_ERR_CUDA;
 
     // fp32 keys run their own kernel mode.
-    const int kmode = (mode == kModeFused && in_dtype == GDR_F32) ? kModeF32Keys : mode;
+    const int kmode = (mode == kModeFused && in_dtype == GDR_F32)
+                          ? (out_dtype == GDR_BF16 ? kModeF32KeysTf32 : kModeF32Keys)
+                          : mode;
     // Input tiles: 64 rows x 128 bytes per box (64 bf16/fp16 key columns, or 32
     // fp32 columns of keys or of A), 128-byte swizzle.
     CUtensorMap tmap;
@@ -1998,7 +2018,7 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     prm.g = mode == kModeSolve ? nullptr : g;
     prm.beta = mode == kModeSolve ? nullptr : beta;
     prm.beta_kind = prm.beta ? beta_dtype : GDR_F32;
-    prm.idesc = kmode == kModeF32Keys ? kIdescTf32 : idesc_f16_kind(in_dtype == GDR_BF16);
+    prm.idesc = in_dtype == GDR_F32 ? kIdescTf32 : idesc_f16_kind(in_dtype == GDR_BF16);
     prm.cu = cu_seqlens;
     prm.out = out;
     prm.B = B;
@@ -2033,7 +2053,7 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
         if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
         return GDR_OK;
     }
-    const int nkb = static_cast<int>(kmode == kModeF32Keys ? K / 32 : K / 64);
+    const int nkb = static_cast<int>(in_dtype == GDR_F32 && kmode != kModeSolve ? K / 32 : K / 64);
     kernel_for(kmode, out_kind, nkb)<<<gx, kmode == kModeF32Keys ? kNumThreadsF32Keys : kNumThreads,
                                         kSmemBytes, st>>>(tmap, tmap_o, prm);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;

@@ -90,10 +90,13 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta,
  *
  *   k_dtype    GDR_BF16 or GDR_F16 (the Gram runs on the tensor cores in that
  *              type; products are exact in the fp32 accumulator), or GDR_F32
- *              with K = 64 or 128 and chunk_size 64 (each key is split into a
- *              tf32 part and a tf32 remainder and the Gram takes three tf32
- *              products, about 2^-20 relative error; fp32 keys with other K or
- *              chunk sizes return GDR_ERR_SHAPE or GDR_ERR_DTYPE).
+ *              with K = 64 or 128 and chunk_size 64.  With fp32 or fp16 output
+ *              each key is split into a tf32 part and a tf32 remainder and the
+ *              Gram takes three tf32 products (about 2^-20 relative error);
+ *              with bf16 output the Gram is one tf32 product of the keys as
+ *              given (each key element narrowed by at most 2^-10 of itself,
+ *              below the output's own rounding).  fp32 keys with other K or
+ *              chunk sizes return GDR_ERR_SHAPE or GDR_ERR_DTYPE.
  *   chunk_size 64, or 128 (K = 64 or 128; bf16 or fp16 keys): out is then
  *              [B, T, H, 128] and each 128-token chunk is one problem, as in
  *              the PyPTO page "GatedDeltaRule算子性能优化案例", section 3.2.

@@ -118,8 +118,9 @@ def test_fp16_all_inputs_fp16_output_large_k():
 @pytest.mark.parametrize("K", [64, 128])
 @pytest.mark.parametrize("layout,out_name", [("fixed", "f32"), ("varlen", "f32"), ("fixed", "bf16")])
 def test_fp32_keys(K, layout, out_name):
-    # fp32 keys: the Gram is formed from tf32 parts and remainders (three tf32
-    # products), so fp32 output still meets the fp32 tolerance.
+    # fp32 keys: for fp32 (and fp16) output the Gram is formed from tf32 parts
+    # and remainders (three tf32 products), so fp32 output still meets the fp32
+    # tolerance; bf16 output takes one tf32 product (see below).
     if layout == "fixed":
         wl = workloads.Workload(f"f32keys_K{K}", 2, 300, 5, K, out_name, seed=800 + K, k_dtype="f32")
     else:
@@ -130,3 +131,31 @@ def test_fp32_keys(K, layout, out_name):
 
 def test_fp32_keys_many_pairs_per_cta():
     _parity(workloads.Workload("f32keys_large", 2, 4096, 16, 128, "f32", seed=820, k_dtype="f32"), "f32")
+
+
+@pytest.mark.parametrize("K", [64, 128])
+def test_fp32_keys_fp16_output(K):
+    # fp16 output takes the split Gram too: one fp16 rounding of an fp32-accurate
+    # result.
+    wl = workloads.Workload(f"f32keys_K{K}_f16", 2, 300, 5, K, "f16", seed=830 + K, k_dtype="f32",
+                            beta_dtype="f16")
+    _parity(wl, "f16")
+
+
+@pytest.mark.parametrize("K,layout", [(64, "fixed"), (128, "varlen"), (128, "large")])
+def test_fp32_keys_bf16_output_one_tf32_product(K, layout):
+    # bf16 output takes one tf32 product of the keys as given: each key element is
+    # narrowed by at most 2^-10 of itself, far below the output's own rounding
+    # (2^-9 |ref|).  Besides the bf16 tolerance every bf16 output meets, the mean
+    # error must stay at that rounding's scale (a dropped K part or a wrong box
+    # would put it orders of magnitude higher).
+    if layout == "fixed":
+        wl = workloads.Workload(f"f32keys_K{K}_bf16", 3, 1000, 4, K, "bf16", seed=840 + K, k_dtype="f32")
+    elif layout == "varlen":
+        wl = workloads.Workload(f"f32keys_K{K}_bf16_varlen", len(VARLEN_LENS), sum(VARLEN_LENS), 3, K, "bf16",
+                                seed=850 + K, varlen_lengths=VARLEN_LENS, k_dtype="f32", beta_dtype="f32")
+    else:
+        wl = workloads.Workload(f"f32keys_K{K}_bf16_large", 2, 4096, 16, K, "bf16", seed=860 + K, k_dtype="f32")
+    got, ref = _parity(wl, "bf16")
+    mean_rel = np.abs(got - ref).sum() / np.abs(ref).sum()
+    assert mean_rel <= 2.0 ** -8, (wl.name, mean_rel)
