@@ -69,10 +69,14 @@ constexpr int kNumThreadsF32Keys = kNumThreads + 64;
 
 constexpr int kBoxBytes = kChunk * 64 * 2;          // one (tile, K-half) box: 64 rows x 128 B
 constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][128 B] = 32 KB
-constexpr int kAPitch = 68;                         // floats per A row (68*4 = 272 B)
-constexpr int kATileBytes = kChunk * kAPitch * 4;   // 17408
-constexpr int kATile1Off = kATileBytes + 16;        // second tile shifted by 16 B (other banks)
-constexpr int kAWGBytes = 35840;                    // >= kATile1Off + kATileBytes, multiple of 1024
+// Row r of a 64 x 64 fp32 matrix (A, then X) in shared memory starts at float
+// a_row<P>(r): P = 72 puts it at 72 r + (r & 4), P = 68 at 68 r (see a_row).
+// The 64-token kernel takes P = 72 for bf16 output and 68 otherwise (there the
+// wider rows cost registers the split merge needs); its buffers fit either.
+constexpr int kAPitch = 72;                         // the larger row pitch, for buffer sizes
+constexpr int kATileBytes = kChunk * kAPitch * 4;   // 18432
+constexpr int kATile1Off = kATileBytes;
+constexpr int kAWGBytes = 36864;                    // >= kATile1Off + kATileBytes, multiple of 1024
 constexpr int kStage1Off = 17408;                   // output staging of the second tile (1024-aligned)
 constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
 constexpr uint32_t kTmemCols = 512;
@@ -404,6 +408,22 @@ __device__ __forceinline__ Tile walk_tile(const Params &p, const TileWalk &w) {
 // -(sum_M Z_JM A_IM^T) D_II^T, so every product's left operand is the previous
 // product's accumulator.
 
+// Bank layout of the matrix rows.  With P = 72 rows start 72 r + (r & 4) floats
+// apart: eight consecutive rows begin in eight different 4-bank groups (the
+// row-per-lane float4 writes and reads), and the merge's float2 operand reads
+// (rows 8 nt + g of one half-warp, columns 2 t, 2 t + 1) cover all 32 banks; its
+// transposed scalar reads (rows 2 t and 2 t + 1, columns g) are 2-way.  With
+// P = 68 the scalar reads are conflict-free and the float2 reads 2-way; the
+// chunk-128 kernel (no room for wider rows) and the 64-token kernel's fp32 and
+// fp16 outputs (whose split merge needs the registers the wider addressing
+// takes) keep it.  A block row r0 + x with r0 a multiple of 16 starts at
+// a_row(r0) + a_row(x) in both layouts.
+template <int P>
+__device__ __forceinline__ int a_row(int r) {
+    static_assert(P == 68 || P == 72, "matrix row layouts");
+    return P == 72 ? r * 72 + (r & 4) : r * 68;
+}
+
 // Diagonal inverses are parked in the free upper blocks of the A buffer:
 // D_00 -> block (0,1), D_11 -> (0,2), D_22 -> (0,3), D_33 -> (1,2).
 __device__ __forceinline__ int dslot_r(int I) { return I == 3 ? 1 : 0; }
@@ -412,6 +432,7 @@ __device__ __forceinline__ int dslot_c(int I) { return I == 3 ? 2 : I + 1; }
 // Row c of D_II by right-looking substitution inside block (I, I): y[j]
 // accumulates -sum_{i>j} A[i][j] y[i]; processing i downwards, y[i] is final
 // (plus 1 on the diagonal) when reached.  Rows above c give y = 0.
+template <int P>
 __device__ __forceinline__ void diag_inverse_row(const float *Ab, int c, float (&y)[16]) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) y[j] = 0.0f;
@@ -420,7 +441,7 @@ __device__ __forceinline__ void diag_inverse_row(const float *Ab, int c, float (
         const int i = 15 - ii;
         y[i] += (i == c) ? 1.0f : 0.0f;
         const float yi = y[i];
-        const float4 *Ar = reinterpret_cast<const float4 *>(Ab + i * kAPitch);
+        const float4 *Ar = reinterpret_cast<const float4 *>(Ab + a_row<P>(i));
 #pragma unroll
         for (int j4 = 0; j4 < (i + 3) / 4; ++j4) {
             const float4 a = Ar[j4];
@@ -479,18 +500,17 @@ __device__ __forceinline__ void frag_from_acc(const float (&acc)[2][4], Frag16 &
 
 // acc += F * Bm for a 16x16 right operand Bm read from shared memory: for k8
 // step ks, n8 tile nt and this lane (g = lane / 4, t = lane % 4) the pair
-// (Bm[8ks + 2t][8nt + g], Bm[8ks + 2t + 1][8nt + g]) is the float2 at
-// rowp + (8 nt + g) * kAPitch + 8 ks + 2 t, i.e. Bm is the transpose of the
-// row-major 16x16 block at rowp.
-template <bool SPLIT>
+// (Bm[8ks + 2t][8nt + g], Bm[8ks + 2t + 1][8nt + g]) is the float2 in block row
+// 8 nt + g at column 8 ks + 2 t, i.e. Bm is the transpose of the row-major
+// 16x16 block at rowp.
+template <bool SPLIT, int P>
 __device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag16 &f,
                                                   const float *rowp, int g, int t) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const float2 b = *reinterpret_cast<const float2 *>(rowp + (8 * nt + g) * kAPitch +
-                                                               8 * ks + 2 * t);
+            const float2 b = *reinterpret_cast<const float2 *>(rowp + a_row<P>(8 * nt + g) + 8 * ks + 2 * t);
             if (SPLIT) {
                 uint32_t bb0, bs0, bb1, bs1;
                 split_tf32(b.x, bb0, bs0);
@@ -506,13 +526,24 @@ __device__ __forceinline__ void mma3_times_blockT(float (&acc)[2][4], const Frag
 }
 
 // Left operand D_JJ^T (= Z_JJ) read from its parking block.
-template <bool SPLIT>
+template <bool SPLIT, int P>
 __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag16 &f) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const float v[4] = {D[(8 * ks + 2 * t) * kAPitch + g], D[(8 * ks + 2 * t) * kAPitch + g + 8],
-                            D[(8 * ks + 2 * t + 1) * kAPitch + g],
-                            D[(8 * ks + 2 * t + 1) * kAPitch + g + 8]};
+        // Row 8 ks + 2 t is even, so the next row starts P floats later in both layouts.
+        float v[4];
+        if constexpr (P == 68) {
+            v[0] = D[(8 * ks + 2 * t) * P + g];
+            v[1] = D[(8 * ks + 2 * t) * P + g + 8];
+            v[2] = D[(8 * ks + 2 * t + 1) * P + g];
+            v[3] = D[(8 * ks + 2 * t + 1) * P + g + 8];
+        } else {
+            const float *r0 = D + a_row<P>(8 * ks + 2 * t);
+            v[0] = r0[g];
+            v[1] = r0[g + 8];
+            v[2] = r0[P + g];
+            v[3] = r0[P + g + 8];
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             if (SPLIT) split_tf32(v[e], f.big[ks][e], f.small[ks][e]);
@@ -523,7 +554,7 @@ __device__ __forceinline__ void frag_from_dT(const float *D, int g, int t, Frag1
 
 // Blocks Z_JI = X_IJ^T for I = J+1..3 of one tile (At = its A buffer).  Split
 // operands are rebuilt when needed instead of cached, to stay within registers.
-template <int J, bool SPLIT>
+template <int J, bool SPLIT, int P>
 __device__ __forceinline__ void merge_column(const float *At, int g, int t,
                                              float (&Z)[3 - J][2][4]) {
 #pragma unroll
@@ -532,14 +563,14 @@ __device__ __forceinline__ void merge_column(const float *At, int g, int t,
 #pragma unroll
         for (int M = J; M < I; ++M) {
             Frag16 f;
-            if (M == J) frag_from_dT<SPLIT>(At + 16 * dslot_r(J) * kAPitch + 16 * dslot_c(J), g, t, f);
+            if (M == J) frag_from_dT<SPLIT, P>(At + a_row<P>(16 * dslot_r(J)) + 16 * dslot_c(J), g, t, f);
             else frag_from_acc<SPLIT>(Z[M - J - 1], f);
-            mma3_times_blockT<SPLIT>(acc, f, At + 16 * I * kAPitch + 16 * M, g, t);
+            mma3_times_blockT<SPLIT, P>(acc, f, At + a_row<P>(16 * I) + 16 * M, g, t);
         }
         Frag16 rf;
         frag_from_acc<SPLIT>(acc, rf);
         float z[2][4] = {};
-        mma3_times_blockT<SPLIT>(z, rf, At + 16 * dslot_r(I) * kAPitch + 16 * dslot_c(I), g, t);
+        mma3_times_blockT<SPLIT, P>(z, rf, At + a_row<P>(16 * dslot_r(I)) + 16 * dslot_c(I), g, t);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -650,15 +681,16 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Writes Z_JI (accumulator layout) into rows 16I.. / columns 16J.. of X.
+template <int P>
 __device__ __forceinline__ void store_block_T(float *At, int I, int J, const float (&z)[2][4],
                                               int g, int t) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-        float *r0 = At + (16 * I + 8 * nt + 2 * t) * kAPitch + 16 * J + g;
+        float *r0 = At + a_row<P>(16 * I + 8 * nt + 2 * t) + 16 * J + g;   // even row: next at + P
         r0[0] = z[nt][0];
-        r0[kAPitch] = z[nt][1];
+        r0[P] = z[nt][1];
         r0[8] = z[nt][2];
-        r0[kAPitch + 8] = z[nt][3];
+        r0[P + 8] = z[nt][3];
     }
 }
 
@@ -750,6 +782,7 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
     static_assert(MODE != kModeSolve || NKB == 2, "an A tile row is two 128-byte boxes");
     constexpr bool kUseTmem = MODE != kModeSolve;
     constexpr bool kF32Keys = MODE == kModeF32Keys;
+    constexpr int kP = OUT == kOutBF16 ? 72 : 68;    // A buffer row layout (a_row)
     // Elements per 128-byte box row: 64 bf16/fp16 key columns, or 32 fp32 ones.
     constexpr bool kTf32Gram = MODE == kModeF32KeysTf32;
     constexpr int kBoxCols = (MODE == kModeSolve || kF32Keys || kTf32Gram) ? 32 : 64;
@@ -1078,7 +1111,7 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                 // Every thread acquires the stage's completed phase itself.
                 if (!mbar_wait(bar_in, static_cast<uint32_t>(r & 1))) record_timeout(p, abort_flag);
                 const uint8_t *sa = smem + kOffK + wg * kStageBytes + tt_e * kBoxBytes + i_e * 128;
-                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + i_e * kAPitch);
+                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + a_row<kP>(i_e));
                 const int n4 = (qd & 1) ? 16 : 8;
 #pragma unroll
                 for (int j4 = 0; j4 < 16; ++j4) {
@@ -1108,7 +1141,7 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
 
-                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + i_e * kAPitch);
+                float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + a_row<kP>(i_e));
                 // Rows 0..31 only need columns j < 32 (A is strictly lower).  The
                 // kkt mode writes whole rows, zero at and above the diagonal.
                 const int n4 = (MODE == kModeKkt || (qd & 1)) ? 16 : 8;
@@ -1174,9 +1207,9 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                 // ---- diagonal inverses: thread -> (tile, block I, row c)
                 const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
                 float drow[16];
-                diag_inverse_row(At(dt) + 16 * dI * (kAPitch + 1), dc, drow);
+                diag_inverse_row<kP>(At(dt) + a_row<kP>(16 * dI) + 16 * dI, dc, drow);
                 {
-                    float4 *dst = reinterpret_cast<float4 *>(At(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
+                    float4 *dst = reinterpret_cast<float4 *>(At(dt) + a_row<kP>(16 * dslot_r(dI) + dc) +
                                                              16 * dslot_c(dI));
     #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4)
@@ -1190,15 +1223,15 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                 uint8_t *const st_m = abuf + (mt ? kStage1Off : 0);
                 if (qd < 2) {
                     float z0[3][2][4];
-                    merge_column<0, OUT != kOutBF16>(At(mt), g8, t4, z0);
+                    merge_column<0, OUT != kOutBF16, kP>(At(mt), g8, t4, z0);
                     named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
                     stage_block_T<OUT>(st_m, 1, 0, z0[0], g8, t4);
                     stage_block_T<OUT>(st_m, 2, 0, z0[1], g8, t4);
                     stage_block_T<OUT>(st_m, 3, 0, z0[2], g8, t4);
                 } else {
                     float z1[2][2][4], z2[1][2][4];
-                    merge_column<1, OUT != kOutBF16>(At(mt), g8, t4, z1);
-                    merge_column<2, OUT != kOutBF16>(At(mt), g8, t4, z2);
+                    merge_column<1, OUT != kOutBF16, kP>(At(mt), g8, t4, z1);
+                    merge_column<2, OUT != kOutBF16, kP>(At(mt), g8, t4, z2);
                     named_bar_sync(bar_id, 128);                   // B4: A and D no longer read
                     stage_block_T<OUT>(st_m, 2, 1, z1[0], g8, t4);
                     stage_block_T<OUT>(st_m, 3, 1, z1[1], g8, t4);
@@ -1276,7 +1309,8 @@ constexpr int kC128Stages = 2;
 constexpr int kC128Producer = 4 * kC128WG;
 constexpr int kC128Mma = 4 * kC128WG + 1;
 constexpr int kC128Threads = 32 * (4 * kC128WG + 2);
-constexpr int kMatBytes = kChunk * kAPitch * 4;           // 17408
+constexpr int kC128Pitch = 68;                             // matrix rows 68 floats apart
+constexpr int kMatBytes = kChunk * kC128Pitch * 4;        // 17408
 constexpr int kC128M1Off = kMatBytes + 16;                // other banks than M0
 constexpr int kC128M2Off = 2 * kMatBytes + 32;
 constexpr int kC128WGBytes = kC128M2Off + kMatBytes;       // 52256 (16-byte aligned matrices)
@@ -1469,7 +1503,7 @@ __global__ void __launch_bounds__(kC128Threads, 1)
         float *const M1 = reinterpret_cast<float *>(mb + kC128M1Off);
         float *const M2 = reinterpret_cast<float *>(mb + kC128M2Off);
         auto Mh = [M0, M1](int t) { return t ? M1 : M0; };
-        auto blk = [](float *M, int I, int J) { return M + 16 * I * kAPitch + 16 * J; };
+        auto blk = [](float *M, int I, int J) { return M + 16 * I * kC128Pitch + 16 * J; };
         float *gbuf = reinterpret_cast<float *>(smem + kC128OffG + wg * kC128GBytes);   // [parity][128]
         float *vbuf = gbuf + 2 * 128;
         const int bar_id = 1 + wg;
@@ -1524,7 +1558,7 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                 const int npass = hf ? 2 : 1;
                 for (int pass = 0; pass < npass; ++pass) {
                     const int cb = pass == 0 ? 64 * hf : 0;        // TMEM columns = partner rows
-                    float *const Arowf = (pass == 0 ? Mh(hf) : M2) + ih * kAPitch;
+                    float *const Arowf = (pass == 0 ? Mh(hf) : M2) + ih * kC128Pitch;
                     // Diagonal block rows 0..31 only need columns j < 32.
                     const int nh = (pass == 1 || (qd & 1)) ? 2 : 1;
                     for (int hh = 0; hh < nh; ++hh) {              // 32 columns at a time
@@ -1576,9 +1610,9 @@ __global__ void __launch_bounds__(kC128Threads, 1)
             // ---- diagonal inverses: thread -> (half, block, row) as in the 64 kernel
             const int dt = tid >> 6, dI = (tid >> 4) & 3, dc = tid & 15;
             float drow[16];
-            diag_inverse_row(Mh(dt) + 16 * dI * (kAPitch + 1), dc, drow);
+            diag_inverse_row<kC128Pitch>(Mh(dt) + 16 * dI * (kC128Pitch + 1), dc, drow);
             {
-                float4 *dst = reinterpret_cast<float4 *>(Mh(dt) + (16 * dslot_r(dI) + dc) * kAPitch +
+                float4 *dst = reinterpret_cast<float4 *>(Mh(dt) + (16 * dslot_r(dI) + dc) * kC128Pitch +
                                                          16 * dslot_c(dI));
 #pragma unroll
                 for (int j4 = 0; j4 < 4; ++j4)
@@ -1591,22 +1625,22 @@ __global__ void __launch_bounds__(kC128Threads, 1)
             const int mt = qd & 1;
             if (qd < 2) {
                 float z0[3][2][4];
-                merge_column<0, SPLIT>(Mh(mt), g8, t4, z0);
+                merge_column<0, SPLIT, kC128Pitch>(Mh(mt), g8, t4, z0);
                 named_bar_sync(bar_id, 128);                   // A11, A22 no longer read
-                store_block_T(Mh(mt), 1, 0, z0[0], g8, t4);
-                store_block_T(Mh(mt), 2, 0, z0[1], g8, t4);
-                store_block_T(Mh(mt), 3, 0, z0[2], g8, t4);
+                store_block_T<kC128Pitch>(Mh(mt), 1, 0, z0[0], g8, t4);
+                store_block_T<kC128Pitch>(Mh(mt), 2, 0, z0[1], g8, t4);
+                store_block_T<kC128Pitch>(Mh(mt), 3, 0, z0[2], g8, t4);
             } else {
                 float z1[2][2][4], z2[1][2][4];
-                merge_column<1, SPLIT>(Mh(mt), g8, t4, z1);
-                merge_column<2, SPLIT>(Mh(mt), g8, t4, z2);
+                merge_column<1, SPLIT, kC128Pitch>(Mh(mt), g8, t4, z1);
+                merge_column<2, SPLIT, kC128Pitch>(Mh(mt), g8, t4, z2);
                 named_bar_sync(bar_id, 128);                   // A11, A22 no longer read
-                store_block_T(Mh(mt), 2, 1, z1[0], g8, t4);
-                store_block_T(Mh(mt), 3, 1, z1[1], g8, t4);
-                store_block_T(Mh(mt), 3, 2, z2[0], g8, t4);
+                store_block_T<kC128Pitch>(Mh(mt), 2, 1, z1[0], g8, t4);
+                store_block_T<kC128Pitch>(Mh(mt), 3, 1, z1[1], g8, t4);
+                store_block_T<kC128Pitch>(Mh(mt), 3, 2, z2[0], g8, t4);
             }
             {
-                float4 *dst = reinterpret_cast<float4 *>(Mh(dt) + (16 * dI + dc) * kAPitch + 16 * dI);
+                float4 *dst = reinterpret_cast<float4 *>(Mh(dt) + (16 * dI + dc) * kC128Pitch + 16 * dI);
 #pragma unroll
                 for (int j4 = 0; j4 < 4; ++j4)
                     dst[j4] = make_float4(drow[4 * j4], drow[4 * j4 + 1], drow[4 * j4 + 2], drow[4 * j4 + 3]);
@@ -1631,14 +1665,14 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                     for (int K2 = 0; K2 < 4; ++K2) {
                         if (K2 >= J) {
                             Frag16 f;
-                            frag_from_dT<SPLIT>(blk(M0, K2, J), g8, t4, f);
-                            mma3_times_blockT<SPLIT>(pt[J], f, blk(M2, M, K2), g8, t4);
+                            frag_from_dT<SPLIT, kC128Pitch>(blk(M0, K2, J), g8, t4, f);
+                            mma3_times_blockT<SPLIT, kC128Pitch>(pt[J], f, blk(M2, M, K2), g8, t4);
                         }
                     }
                 }
                 __syncwarp();
 #pragma unroll
-                for (int J = 0; J < 4; ++J) store_block_T(M2, M, J, pt[J], g8, t4);
+                for (int J = 0; J < 4; ++J) store_block_T<kC128Pitch>(M2, M, J, pt[J], g8, t4);
             }
             named_bar_sync(bar_id, 128);                       // P complete
             {
@@ -1654,8 +1688,8 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                     for (int M = 0; M < 4; ++M) {
                         if (M <= I) {
                             Frag16 f;
-                            frag_from_dT<SPLIT>(blk(M2, M, J), g8, t4, f);
-                            mma3_times_blockT<SPLIT>(xt[I], f, blk(M1, I, M), g8, t4);
+                            frag_from_dT<SPLIT, kC128Pitch>(blk(M2, M, J), g8, t4, f);
+                            mma3_times_blockT<SPLIT, kC128Pitch>(xt[I], f, blk(M1, I, M), g8, t4);
                         }
                     }
                 }
@@ -1666,7 +1700,7 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) xt[I][nt][e] = -xt[I][nt][e];
-                    store_block_T(M2, I, J, xt[I], g8, t4);
+                    store_block_T<kC128Pitch>(M2, I, J, xt[I], g8, t4);
                 }
             }
             named_bar_sync(bar_id, 128);                       // X complete
@@ -1692,13 +1726,13 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                     const float *src;
                     bool zero = false, mask = true;
                     if (rr < 64) {
-                        src = M0 + rh * kAPitch + cc;
+                        src = M0 + rh * kC128Pitch + cc;
                         zero = right;
                     } else if (!right) {
-                        src = M2 + rh * kAPitch + cc;
+                        src = M2 + rh * kC128Pitch + cc;
                         mask = false;
                     } else {
-                        src = M1 + rh * kAPitch + cc;
+                        src = M1 + rh * kC128Pitch + cc;
                     }
 #pragma unroll
                     for (int e4 = 0; e4 < kCols / 4; ++e4) {
