@@ -24,6 +24,10 @@
  *     and then nothing is enqueued and `out` is untouched.
  *   - Calls are thread-safe (no mutable host state besides a once-initialised
  *     driver entry point).
+ *   - After one call on a device (which sets up the library's per-device state
+ *     outside any capture), calls on that device can be captured into a CUDA
+ *     graph by stream capture; a replay reads the input buffers as they are at
+ *     replay time.
  */
 #ifndef GDR_KKT_SOLVE_H
 #define GDR_KKT_SOLVE_H
