@@ -33,7 +33,8 @@ GDR_BF16 = 1
 GDR_F16 = 2
 
 EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_kkt_solve_ex", "gdr_chunk_scaled_dot_kkt",
-                    "gdr_solve_tril", "gdr_kkt_solve_unfused_noalloc", "gdr_status_string",
+                    "gdr_solve_tril", "gdr_kkt_solve_unfused_noalloc", "gdr_kkt_solve_host",
+                    "gdr_kkt_solve_host_workspace_bytes", "gdr_status_string",
                     "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms", "gdr_selftest_bounded_wait")
 
 _lib = None
@@ -75,6 +76,11 @@ def load_library():
             lib.gdr_kkt_solve_unfused_noalloc.argtypes = [vp, ci, vp, vp, ci, vp, i64, i64, i64, i64, ci, ci,
                                                           vp, vp]
             lib.gdr_kkt_solve_unfused_noalloc.restype = ci
+            lib.gdr_kkt_solve_host.argtypes = [vp, ci, vp, vp, ci, vp, i64, i64, i64, i64, ci, ci, vp, vp, i64,
+                                               vp]
+            lib.gdr_kkt_solve_host.restype = ci
+            lib.gdr_kkt_solve_host_workspace_bytes.argtypes = [ci, i64, i64, i64, i64, ci, ci]
+            lib.gdr_kkt_solve_host_workspace_bytes.restype = i64
             lib.gdr_status_string.argtypes = [ci]
             lib.gdr_status_string.restype = ctypes.c_char_p
             lib.gdr_kkt_solve_device_status.argtypes = [ctypes.POINTER(ci)]
@@ -135,6 +141,25 @@ def kkt_solve_unfused_noalloc_raw(k_ptr: int, k_dtype: int, g_ptr: int, beta_ptr
                                                         beta_ptr or None, beta_dtype, cu_ptr or None,
                                                         B, T, H, K, chunk_size, out_dtype,
                                                         out_ptr or None, stream or None)
+
+
+def kkt_solve_host_raw(k_ptr: int, k_dtype: int, g_ptr: int, beta_ptr: int, beta_dtype: int, cu_ptr: int,
+                       B: int, T: int, H: int, K: int, chunk_size: int, out_dtype: int, out_ptr: int,
+                       ws_ptr: int, ws_bytes: int, stream: int) -> int:
+    """Direct call of gdr_kkt_solve_host (host input and output pointers, a device
+    workspace); returns the gdr_status code."""
+    return load_library().gdr_kkt_solve_host(k_ptr or None, k_dtype, g_ptr or None, beta_ptr or None,
+                                             beta_dtype, cu_ptr or None, B, T, H, K, chunk_size, out_dtype,
+                                             out_ptr or None, ws_ptr or None, ws_bytes, stream or None)
+
+
+def kkt_solve_host_workspace_bytes(k_dtype: int, B: int, T: int, H: int, K: int, chunk_size: int,
+                                   out_dtype: int) -> int:
+    """Device workspace bytes gdr_kkt_solve_host needs (raises on invalid arguments)."""
+    n = load_library().gdr_kkt_solve_host_workspace_bytes(k_dtype, B, T, H, K, chunk_size, out_dtype)
+    if n < 0:
+        raise GdrError(int(n), "gdr_kkt_solve_host_workspace_bytes")
+    return int(n)
 
 
 def _gdr_dtype(dt, what: str) -> int:
@@ -221,6 +246,59 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
                               B, T, H, K, chunk_size, out_code, out.data_ptr(), int(stream))
     if rc != GDR_OK:
         raise GdrError(rc, "gdr_kkt_solve_ex")
+    return out
+
+
+def kkt_solve_host(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, output_dtype=None,
+                   out=None, workspace=None, stream=None, device=None):
+    """kkt_solve on HOST tensors (gdr_kkt_solve_host): k, g, beta, cu_seqlens are
+    CPU tensors (page-locked for overlapped copies), out a CPU tensor or None
+    (then a page-locked one is allocated).  `workspace` is a uint8 CUDA tensor of
+    at least kkt_solve_host_workspace_bytes(...) bytes, or None (then one is
+    allocated on `device`, default the current CUDA device).  The call is
+    asynchronous on `stream` (default the device's current stream): synchronise
+    it before reading out.  Returns out [B, T, H, chunk_size]."""
+    import torch
+
+    if output_dtype is None:
+        output_dtype = torch.float32
+    out_code = _gdr_dtype(output_dtype, "output_dtype")
+    if k.dim() != 4 or k.is_cuda:
+        raise TypeError("k must be a 4-D CPU tensor")
+    for name, t in (("g", g), ("beta", beta), ("cu_seqlens", cu_seqlens)):
+        if t is not None and t.is_cuda:
+            raise TypeError(f"{name} must be a CPU tensor")
+    if g is not None and g.dtype != torch.float32:
+        raise TypeError("g must be float32")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    k_code = _gdr_dtype(k.dtype, "k")
+    beta_code = GDR_F32 if beta is None else _gdr_dtype(beta.dtype, "beta")
+    Bk, T, H, K = k.shape
+    B = Bk if cu_seqlens is None else cu_seqlens.numel() - 1
+    k = k.contiguous()
+    g = None if g is None else g.contiguous()
+    beta = None if beta is None else beta.contiguous()
+    cu_seqlens = None if cu_seqlens is None else cu_seqlens.contiguous()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        out = torch.empty((Bk, T, H, chunk_size), dtype=output_dtype, pin_memory=True)
+    elif out.is_cuda or out.dtype != output_dtype or tuple(out.shape) != (Bk, T, H, chunk_size) \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU tensor of the output's dtype and shape")
+    need = kkt_solve_host_workspace_bytes(k_code, B, T, H, K, chunk_size, out_code)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        rc = kkt_solve_host_raw(k.data_ptr(), k_code, 0 if g is None else g.data_ptr(),
+                                0 if beta is None else beta.data_ptr(), beta_code,
+                                0 if cu_seqlens is None else cu_seqlens.data_ptr(), B, T, H, K, chunk_size,
+                                out_code, out.data_ptr(), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), int(stream))
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_kkt_solve_host")
     return out
 
 

@@ -1,4 +1,5 @@
-"""In-tree build of the CUDA library (plain nvcc, one translation unit, sm_103a only)."""
+"""In-tree build of the CUDA library (plain nvcc, sm_103a only): the kernels and
+their entry points in one translation unit, the host-buffer entry in another."""
 from __future__ import annotations
 
 import os
@@ -12,7 +13,7 @@ CSRC_DIR = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libgdr_kkt_solve.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = [os.path.join(CSRC_DIR, "gdr_kkt_solve.cu")]
+SOURCES = [os.path.join(CSRC_DIR, "gdr_kkt_solve.cu"), os.path.join(CSRC_DIR, "gdr_host.cpp")]
 HEADERS = [os.path.join(INCLUDE_DIR, "gdr_kkt_solve.h")]
 
 NVCC_FLAGS = [

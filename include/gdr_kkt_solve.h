@@ -173,6 +173,44 @@ int gdr_kkt_solve_unfused_noalloc(const void *k, int k_dtype, const float *g, co
                                   int64_t H, int64_t K, int chunk_size, int out_dtype, void *out,
                                   void *stream);
 
+/*
+ * gdr_kkt_solve_host - gdr_kkt_solve_ex on HOST buffers (no counterpart on the
+ * pages; for callers whose inputs and output live in host memory).  k, g, beta,
+ * cu_seqlens and out are host pointers with the layouts of gdr_kkt_solve_ex;
+ * `workspace` is a device buffer of at least
+ * gdr_kkt_solve_host_workspace_bytes(k_dtype, B, T, H, K, chunk_size,
+ * out_dtype) bytes, 256-byte aligned, owned by the caller (the library still
+ * allocates no device memory).  The call copies the inputs into the workspace,
+ * runs the kernel and copies the output back, slice by slice (runs of whole
+ * chunks of one sequence) over two internal streams, so that host-to-device
+ * copies, kernels and device-to-host copies of different slices overlap;
+ * packed sequences (cu_seqlens) go as one slice, and then only the rows of
+ * real tokens are written to out.  The work is ordered after everything
+ * enqueued on `stream` before the call, and everything enqueued on `stream`
+ * afterwards waits for it (synchronise `stream` before reading out).  The
+ * result equals gdr_kkt_solve_ex's, bit for bit whenever every chunk's
+ * log-gate lies within 30 of the midpoint of its first and last value (the
+ * kernel's factored gate), else to rounding.
+ *   Host memory: page-locked buffers let the copies run asynchronously and
+ *          overlap; pageable ones work, without the overlap.
+ *   Streams: the two internal streams and three events per device are created
+ *          on the first call on that device and kept until exit.  Calls on one
+ *          device enqueue one at a time.  The call is not meant for stream
+ *          capture.
+ *   Errors: every check of gdr_kkt_solve_ex, plus GDR_ERR_NULL (workspace),
+ *          GDR_ERR_SHAPE (workspace too small), GDR_ERR_ALIGN (workspace), all
+ *          before anything is enqueued.
+ */
+int gdr_kkt_solve_host(const void *k, int k_dtype, const float *g, const void *beta, int beta_dtype,
+                       const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H, int64_t K, int chunk_size,
+                       int out_dtype, void *out, void *workspace, int64_t workspace_bytes, void *stream);
+
+/* Device workspace bytes gdr_kkt_solve_host needs (for fixed-length and packed
+ * inputs alike; room for beta in any type), or a negative gdr_status for
+ * invalid types or sizes. */
+int64_t gdr_kkt_solve_host_workspace_bytes(int k_dtype, int64_t B, int64_t T, int64_t H, int64_t K,
+                                           int chunk_size, int out_dtype);
+
 /* Human-readable text for a gdr_status value (static storage, never NULL). */
 const char *gdr_status_string(int status);
 

@@ -230,3 +230,49 @@ def test_noalloc_within_limit_reaches_the_device_check():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; this test covers the no-device path")
     assert _call_noalloc(B=1, T=1 << 16, H=4) == gdr.GDR_ERR_DEVICE     # exactly 262144
+
+
+# gdr_kkt_solve_host: host pointers (any readable host address works for the
+# checks, which happen before anything is enqueued) and a device workspace.
+HOST_BUF = ctypes.create_string_buffer(4096 + 256)
+HOST_PTR = (ctypes.addressof(HOST_BUF) + 255) // 256 * 256
+WS_PTR = 1 << 40                      # 256-byte aligned stand-in device address
+
+
+def _call_host(**kw):
+    a = dict(k=HOST_PTR, kd=gdr.GDR_BF16, g=HOST_PTR, beta=HOST_PTR, bd=gdr.GDR_BF16, cu=0, B=2, T=100, H=3,
+             K=128, chunk=64, dtype=gdr.GDR_F32, out=HOST_PTR, ws=WS_PTR, wsb=None)
+    a.update(kw)
+    if a["wsb"] is None:
+        a["wsb"] = gdr.kkt_solve_host_workspace_bytes(gdr.GDR_BF16, 2, 100, 3, 128, 64, gdr.GDR_F32)
+    return gdr.kkt_solve_host_raw(a["k"], a["kd"], a["g"], a["beta"], a["bd"], a["cu"], a["B"], a["T"], a["H"],
+                                  a["K"], a["chunk"], a["dtype"], a["out"], a["ws"], a["wsb"], 0)
+
+
+def test_host_workspace_bytes():
+    n = gdr.kkt_solve_host_workspace_bytes(gdr.GDR_BF16, 2, 16384, 32, 128, 64, gdr.GDR_BF16)
+    tok_heads = 2 * 16384 * 32
+    # k, g, beta (fp32 room), cu, out, each 256-byte aligned
+    assert n >= tok_heads * (256 + 4 + 4 + 128) and n % 256 == 0
+    assert n < tok_heads * (256 + 4 + 4 + 128) + 5 * 256 + 4 * 3
+    with pytest.raises(gdr.GdrError):
+        gdr.kkt_solve_host_workspace_bytes(gdr.GDR_BF16, 2, 16, 2, 100, 64, gdr.GDR_F32)
+    with pytest.raises(gdr.GdrError):
+        gdr.kkt_solve_host_workspace_bytes(7, 2, 16, 2, 128, 64, gdr.GDR_F32)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(k=0), gdr.GDR_ERR_NULL), (dict(out=0), gdr.GDR_ERR_NULL), (dict(ws=0), gdr.GDR_ERR_NULL),
+    (dict(wsb=1024), gdr.GDR_ERR_SHAPE), (dict(ws=WS_PTR + 16), gdr.GDR_ERR_ALIGN),
+    (dict(chunk=32), gdr.GDR_ERR_CHUNK), (dict(dtype=9), gdr.GDR_ERR_DTYPE), (dict(kd=9), gdr.GDR_ERR_DTYPE),
+    (dict(K=100), gdr.GDR_ERR_SHAPE), (dict(H=-1), gdr.GDR_ERR_SHAPE),
+    (dict(kd=gdr.GDR_F32, K=256), gdr.GDR_ERR_SHAPE), (dict(T=0), gdr.GDR_OK), (dict(B=0), gdr.GDR_OK)])
+def test_host_entry_argument_checks(kw, want):
+    assert _call_host(**kw) == want
+
+
+def test_host_entry_valid_arguments_reach_the_device_check():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this test covers the no-device path")
+    assert _call_host() == gdr.GDR_ERR_DEVICE
