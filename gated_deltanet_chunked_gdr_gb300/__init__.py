@@ -280,12 +280,12 @@ def kkt_solve_host(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, 
     g = None if g is None else g.contiguous()
     beta = None if beta is None else beta.contiguous()
     cu_seqlens = None if cu_seqlens is None else cu_seqlens.contiguous()
+    if out is not None and (out.is_cuda or out.dtype != output_dtype or tuple(out.shape) != (Bk, T, H, chunk_size)
+                            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous CPU tensor of the output's dtype and shape")
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     if out is None:
         out = torch.empty((Bk, T, H, chunk_size), dtype=output_dtype, pin_memory=True)
-    elif out.is_cuda or out.dtype != output_dtype or tuple(out.shape) != (Bk, T, H, chunk_size) \
-            or not out.is_contiguous():
-        raise ValueError("out must be a contiguous CPU tensor of the output's dtype and shape")
     need = kkt_solve_host_workspace_bytes(k_code, B, T, H, K, chunk_size, out_code)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)

@@ -276,3 +276,16 @@ def test_host_entry_valid_arguments_reach_the_device_check():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; this test covers the no-device path")
     assert _call_host() == gdr.GDR_ERR_DEVICE
+
+
+def test_host_binding_rejects_device_tensors_and_bad_types():
+    import torch
+    k = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        gdr.kkt_solve_host(k, g=torch.zeros(1, 64, 2, dtype=torch.float16))          # g must be fp32
+    with pytest.raises(TypeError):
+        gdr.kkt_solve_host(k, cu_seqlens=torch.tensor([0, 64], dtype=torch.int64))  # cu_seqlens int32
+    with pytest.raises(TypeError):
+        gdr.kkt_solve_host(k.float().double())                                       # fp64 keys
+    with pytest.raises(ValueError):
+        gdr.kkt_solve_host(k, out=torch.empty(1, 64, 2, 32))                          # wrong out shape
