@@ -255,9 +255,11 @@ def kkt_solve_host(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, 
     CPU tensors (page-locked for overlapped copies), out a CPU tensor or None
     (then a page-locked one is allocated).  `workspace` is a uint8 CUDA tensor of
     at least kkt_solve_host_workspace_bytes(...) bytes, or None (then one is
-    allocated on `device`, default the current CUDA device).  The call is
-    asynchronous on `stream` (default the device's current stream): synchronise
-    it before reading out.  Returns out [B, T, H, chunk_size]."""
+    allocated on `device`, default the current CUDA device, and kept from reuse
+    until `stream` has passed the call); a workspace passed in must not be used
+    for anything else until then.  The call is asynchronous on `stream` (default
+    the device's current stream): synchronise it before reading out.  Returns
+    out [B, T, H, chunk_size]."""
     import torch
 
     if output_dtype is None:
@@ -287,7 +289,8 @@ def kkt_solve_host(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, 
     if out is None:
         out = torch.empty((Bk, T, H, chunk_size), dtype=output_dtype, pin_memory=True)
     need = kkt_solve_host_workspace_bytes(k_code, B, T, H, K, chunk_size, out_code)
-    if workspace is None:
+    own_workspace = workspace is None
+    if own_workspace:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev).cuda_stream
@@ -297,6 +300,10 @@ def kkt_solve_host(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, 
                                 0 if cu_seqlens is None else cu_seqlens.data_ptr(), B, T, H, K, chunk_size,
                                 out_code, out.data_ptr(), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), int(stream))
+    if own_workspace:
+        # The call's internal streams use the workspace; the caller's stream waits
+        # for them, so the allocator may reuse it once that stream passes here.
+        workspace.record_stream(torch.cuda.ExternalStream(int(stream), device=dev))
     if rc != GDR_OK:
         raise GdrError(rc, "gdr_kkt_solve_host")
     return out
