@@ -3,9 +3,10 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
 
 One step = one kkt_solve over the whole workload ((2, 16384, 32, 128), bf16 keys,
-bf16 output by default) with inputs already resident in HBM.  The step's
-inputs and output (409 MB) exceed the 129 MB L2, so no flush is needed between
-steps.  Prints one JSON line (rank 0).  Under torchrun every rank runs the same
+bf16 output by default) with inputs already resident in HBM.  The default
+step's inputs and output (409 MB) exceed twice the 129 MB L2, so it is timed
+back to back; a smaller workload is timed cold (a 512 MiB buffer is written
+before each step, and only the steps are timed).  Prints one JSON line (rank 0).  Under torchrun every rank runs the same
 workload on its own GPU (independent replicas: weak scaling, no data-path
 collective); timing is the max over ranks.
 
@@ -45,7 +46,7 @@ ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4}
 
 def bytes_per_token_head(wl, out_dtype: str) -> int:
     """Algorithmic HBM bytes per token-head: read k (K values), g (fp32), beta;
-    write one output row of 64 values."""
+    write one output row of `chunk` values."""
     b = wl.K * ELEM_BYTES[wl.k_dtype]
     b += 4 if wl.use_g else 0
     b += ELEM_BYTES[wl.beta_dtype] if wl.use_beta else 0
@@ -195,7 +196,7 @@ def run_reference(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "K": wl.K, "chunk": 64,
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "K": wl.K, "chunk": wl.chunk,
                    "impl": "plain C fp64 oracle, threads over tiles",
                    "sample_tiles_per_step": per_step},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
