@@ -15,19 +15,22 @@
  * on the lower triangle.
  *
  * Conventions for every entry point below:
- *   - All tensor pointers are DEVICE pointers owned by the caller.  Nothing is
- *     allocated or freed by the library, and nothing is retained after return.
+ *   - All tensor pointers are DEVICE pointers owned by the caller (except for
+ *     gdr_kkt_solve_host, which takes host pointers and a device workspace).
+ *     No device memory is allocated or freed by the library, and no pointer is
+ *     retained after return.
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
  *     legacy default stream) and the call returns without synchronising.
  *   - Errors are returned as gdr_status codes; the library never aborts, traps
  *     or prints.  Argument errors are detected on the host before any launch,
  *     and then nothing is enqueued and `out` is untouched.
- *   - Calls are thread-safe (no mutable host state besides a once-initialised
- *     driver entry point).
+ *   - Calls are thread-safe: the only mutable host state (a driver entry point,
+ *     per-device set-up, the host-buffer call's streams and events) is
+ *     initialised once under a lock.
  *   - After one call on a device (which sets up the library's per-device state
- *     outside any capture), calls on that device can be captured into a CUDA
- *     graph by stream capture; a replay reads the input buffers as they are at
- *     replay time.
+ *     outside any capture), gdr_kkt_solve and gdr_kkt_solve_ex on that device
+ *     can be captured into a CUDA graph by stream capture; a replay reads the
+ *     input buffers as they are at replay time.
  */
 #ifndef GDR_KKT_SOLVE_H
 #define GDR_KKT_SOLVE_H
@@ -42,7 +45,7 @@ typedef enum {
     GDR_OK = 0,
     GDR_ERR_NULL = -1,    /* a required pointer is NULL                        */
     GDR_ERR_SHAPE = -2,   /* negative size, K not in {64,128,192,256}, overflow */
-    GDR_ERR_CHUNK = -3,   /* chunk_size != 64                                  */
+    GDR_ERR_CHUNK = -3,   /* chunk_size not 64 (or 128 for the fused call)      */
     GDR_ERR_DTYPE = -4,   /* a dtype argument outside the supported set        */
     GDR_ERR_ALIGN = -5,   /* a pointer is not aligned as documented below      */
     GDR_ERR_DEVICE = -6,  /* no current CUDA device, or it is not sm_103       */
