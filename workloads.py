@@ -9,11 +9,13 @@ the shapes are the ones quoted on the MindSpeed-Ops PR page "feat(triton): add
 chunk_gated_delta_rule_fwd_kkt_solve", performance table):
   * k    ~ N(0, 1) in fp32, L2-normalised over the head dimension K for every
            (token, head), then rounded to bf16 (round-to-nearest-even), or to
-           fp16 for the fp16-input variants.
+           fp16 for the fp16-input variants, or kept in fp32 for the fp32-key
+           variants.
   * beta = sigmoid(N(0, 1)), rounded to bf16 (or fp16, or kept fp32).
   * g    = per-token U(-0.1, 0) log-decay in fp32, summed inclusively inside
-           every 64-token chunk; the sum restarts at each chunk start, and
-           chunks restart at every sequence start.
+           every chunk (64 tokens, or 128 for the chunk-128 variants); the sum
+           restarts at each chunk start, and chunks restart at every sequence
+           start.
   * varlen: 8 packed sequences with integer lengths ~ U[100, 4000], redrawn
            from the same generator until the total is at most 16384;
            cu_seqlens = [0, cumsum(lengths)] as int32 and k is [1, T, H, K].
@@ -38,12 +40,12 @@ class Workload:
     T: int            # tokens per sequence, or total packed tokens when varlen
     H: int
     K: int
-    out_dtype: str    # "f32" or "bf16"
+    out_dtype: str    # "f32", "bf16" or "f16"
     seed: int
     varlen_lengths: Optional[tuple] = None   # per-sequence lengths when packed
     use_g: bool = True
     use_beta: bool = True
-    k_dtype: str = "bf16"       # "bf16" or "f16": type k is rounded to
+    k_dtype: str = "bf16"       # "bf16" or "f16": type k is rounded to; "f32": kept
     beta_dtype: str = "bf16"    # "bf16", "f16" or "f32"
     chunk: int = CHUNK          # chunk length the log-gate's running sum restarts at
 
