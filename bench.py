@@ -37,6 +37,7 @@ UNIT = "token-heads/s"
 # Ascend 910B fused time for (2,16384,32,128) from the MindSpeed-Ops PR page's
 # performance table: 4.9368 ms -> 1,048,576 token-heads / 4.9368 ms.
 PAGE_FUSED_MS = {"B2_T16384_H32_K128": 4.9368}
+NOMINAL_HBM_GBS = 8000.0             # GB300 HBM3e nominal (~8 TB/s), for the second fraction
 L2_BYTES = 129 * 10**6               # GB300 L2 (two dies together)
 L2_FLUSH_BYTES = 512 << 20           # written before each step of a small workload
 
@@ -163,66 +164,206 @@ class ClockSampler:
 
 
 def run_reference(args, wl):
-    """Reference arm: the fp64 CPU oracle on a bounded sample of tiles per step."""
+    """Reference arm: the fp64 CPU oracle, as it stands, on the host cores.  Each
+    step is the oracle's whole-tensor call (heads split over the host cores) on
+    the workload, or on a token prefix of it when K whole-workload steps would
+    take more than about a minute."""
     import oracle
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     inp = workloads.make_inputs(wl)
-    threads = os.cpu_count() or 1
-    tiles = workloads.tile_list(wl)
-    rng = np.random.default_rng(2024)
-    # Calibrate the per-tile cost, then size each step so K steps take <= ~60 s.
-    calib = [tiles[i] for i in rng.choice(len(tiles), size=min(len(tiles), 4 * threads), replace=False)]
+    threads = min(os.cpu_count() or 1, wl.H)
+    lead = inp["k"].shape[:2]
+    ntok = lead[0] * lead[1]
+    flat = {x: None if inp[x] is None else inp[x].reshape(1, ntok, *inp[x].shape[2:])
+            for x in ("k", "g", "beta")}
+    cu = inp["cu_seqlens"]
+    if cu is None:      # fixed-length sequences, flattened: one packed batch of B sequences
+        cu = np.arange(wl.B + 1, dtype=np.int32) * wl.T
+
+    def run(rows):
+        # Whole sequences up to `rows` tokens (the last one cut at `rows`).
+        c = np.minimum(np.asarray(cu, dtype=np.int64), rows).astype(np.int32)
+        oracle.kkt_solve_ref(flat["k"][:, :rows], None if flat["g"] is None else flat["g"][:, :rows],
+                             None if flat["beta"] is None else flat["beta"][:, :rows], c,
+                             chunk_size=wl.chunk, threads=threads)
+        return int(c[-1]) * wl.H
+
     t0 = time.perf_counter()
-    oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], calib, chunk_size=wl.chunk, threads=threads)
-    per_tile = (time.perf_counter() - t0) / len(calib)
-    per_step = max(1, min(len(tiles), int(60.0 / max(1, args.steps) / per_tile)))
-    samples = [[tiles[i] for i in rng.choice(len(tiles), size=per_step, replace=False)]
-               for _ in range(min(args.steps, 8))]
-    for w in range(args.warmup):
-        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], samples[w % len(samples)],
-                                   chunk_size=wl.chunk, threads=threads)
+    run(ntok)
+    t_whole = time.perf_counter() - t0
+    rows = ntok
+    if t_whole * args.steps > 60.0:
+        rows = max(wl.chunk, int(ntok * 60.0 / (t_whole * args.steps)) // wl.chunk * wl.chunk)
+    for _ in range(args.warmup):
+        run(rows)
     th = 0
     t0 = time.perf_counter()
-    for s in range(args.steps):
-        smp = samples[s % len(samples)]
-        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, chunk_size=wl.chunk, threads=threads)
-        th += sum(t[4] for t in smp)
+    for _ in range(args.steps):
+        th += run(rows)
     dt = time.perf_counter() - t0
     value = th / dt
+    sample = (f"the whole {wl.name} workload per step" if rows == ntok else
+              f"the first {rows} of {ntok} token rows of {wl.name}, all heads, per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "K": wl.K, "chunk": wl.chunk,
-                   "impl": "plain C fp64 oracle, threads over tiles",
-                   "sample_tiles_per_step": per_step},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{per_step} random (chunk, head) tiles of {wl.name} per step"},
+                   "impl": "plain C fp64 oracle, heads split over host threads",
+                   "token_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(wl, inp, budget_s: float):
-    """The oracle, as it stands, on a bounded seeded sample of the workload."""
+def _oracle_prefix(wl, inp, budget_s: float, threads: int):
+    """The oracle's whole-tensor call (heads split over `threads` host threads,
+    each running the plain C loop) on growing token prefixes of the first
+    sequence, all heads, until about `budget_s` seconds of work is done."""
     import oracle
-    threads = os.cpu_count() or 1
-    tiles = workloads.tile_list(wl)
-    rng = np.random.default_rng(7)
-    order = rng.permutation(len(tiles))
-    done, th, t0 = 0, 0, time.perf_counter()
-    batch = 8 * threads
-    while done < len(tiles) and time.perf_counter() - t0 < budget_s:
-        smp = [tiles[i] for i in order[done:done + batch]]
-        oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], smp, chunk_size=wl.chunk, threads=threads)
-        done += len(smp)
-        th += sum(t[4] for t in smp)
-    dt = time.perf_counter() - t0
+    s, e = workloads._sequence_bounds(wl)[0]
+    kf = inp["k"].reshape(-1, wl.H, wl.K)
+    gf = None if inp["g"] is None else inp["g"].reshape(-1, wl.H)
+    bf = None if inp["beta"] is None else inp["beta"].reshape(-1, wl.H)
+    rows, th, dt = min(wl.chunk, e - s), 0, 0.0
+    while True:
+        sl = slice(s, s + rows)
+        t0 = time.perf_counter()
+        oracle.kkt_solve_ref(kf[sl].unsqueeze(0), None if gf is None else gf[sl].unsqueeze(0),
+                             None if bf is None else bf[sl].unsqueeze(0), chunk_size=wl.chunk, threads=threads)
+        t = time.perf_counter() - t0
+        th, dt = rows * wl.H, t
+        if t >= budget_s / 4 or rows >= e - s:
+            return rows, th, dt
+        rows = min(e - s, rows * max(2, int(budget_s / 4 / max(t, 1e-3))) // wl.chunk * wl.chunk or wl.chunk)
+
+
+def _oracle_whole(wl, inp, budget_s: float, threads: int):
+    """The oracle's whole-tensor call on the entire workload, repeated until
+    about `budget_s` seconds have passed (at least once)."""
+    import oracle
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], inp["cu_seqlens"], chunk_size=wl.chunk,
+                             threads=threads)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or dt / n * (n + 1) > 1.5 * budget_s:
+            return n, n * wl.token_heads, dt
+
+
+def cpu_baseline(wl, inp, budget_s: float):
+    """The oracle, as it stands, timed on the host: its whole-tensor call (heads
+    split over the host cores, each thread running the plain C loop) on the
+    entire workload, and on one core on a token prefix of the first sequence."""
+    threads = min(os.cpu_count() or 1, wl.H)
+    n, th, dt = _oracle_whole(wl, inp, budget_s / 2, threads)
+    rows1, th1, dt1 = _oracle_prefix(wl, inp, budget_s / 2, 1)
     return {"value": th / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{done} random (chunk, head) tiles of {wl.name} ({th} token-heads) in {dt:.1f} s"}
+            "sample": f"the whole {wl.name} workload x {n} ({th} token-heads) in {dt:.2f} s, "
+                      f"heads split over {threads} threads",
+            "single_thread": {"value": th1 / dt1, "unit": UNIT, "cores": 1,
+                              "sample": f"first {rows1} tokens x {wl.H} heads ({th1} token-heads) in {dt1:.2f} s"}}
+
+
+def small_workload_lines(dev, stream, gdr, launches: int):
+    """Cold-L2 timings of the smaller workloads, each through the same C-ABI call:
+    a 512 MiB buffer is written before every launch, an event pair times the
+    launch alone; the median is reported, with the warm back-to-back mean."""
+    import torch
+    codes = {"bf16": gdr.GDR_BF16, "f16": gdr.GDR_F16, "f32": gdr.GDR_F32}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    lines = {}
+    for name, out_dtype in (("B1_T256_H8_K128", "f32"), ("B2_T2000_H5_K128", "f32"),
+                            ("B1_T8192_H8_K128", "bf16"), ("B1_T8192_H8_K128", "f32"),
+                            ("varlen8_H16_K128", "f32")):
+        wl = workloads.CONFIGS[name]
+        inp = workloads.make_inputs(wl)
+        k, g, beta = (inp[x].to(dev) for x in ("k", "g", "beta"))
+        cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].to(dev)
+        B = wl.B
+        odt = {"bf16": torch.bfloat16, "f32": torch.float32}[out_dtype]
+        out = torch.empty((*k.shape[:3], 64), dtype=odt, device=dev)
+
+        def step():
+            rc = gdr.kkt_solve_ex_raw(k.data_ptr(), codes[wl.k_dtype], g.data_ptr(), beta.data_ptr(),
+                                      codes[wl.beta_dtype], 0 if cu is None else cu.data_ptr(), B, k.shape[1],
+                                      wl.H, wl.K, 64, codes[out_dtype], out.data_ptr(), stream.cuda_stream)
+            if rc != gdr.GDR_OK:
+                raise gdr.GdrError(rc, "gdr_kkt_solve_ex")
+
+        for _ in range(5):
+            step()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                flush.fill_(1.0)
+                a.record(stream)
+                step()
+                b.record(stream)
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0.record(stream)
+            for _ in range(launches):
+                step()
+            w1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+        med = statistics.median(us)
+        th = wl.token_heads
+        lines[f"{name}:{out_dtype}"] = {
+            "token_heads": th, "cold_median_us": med, "cold_p10_us": us[int(0.1 * (len(us) - 1))],
+            "cold_p90_us": us[int(0.9 * (len(us) - 1))], "warm_mean_us": w0.elapsed_time(w1) * 1e3 / launches,
+            "value": th / (med * 1e-6), "unit": UNIT,
+            "hbm_gbs_cold": th * bytes_per_token_head(wl, out_dtype) / (med * 1e-6) / 1e9,
+            "launches": launches}
+    if gdr.device_status() != gdr.GDR_OK:
+        raise RuntimeError("device status not ok after the small workloads")
+    return lines
+
+
+def link_bound(dev, tensors_h2d, tensors_d2h, reps: int = 5):
+    """Plain page-locked copies of the step's own bytes, one cudaMemcpyAsync per
+    tensor (torch's non-blocking copy): host-to-device alone, device-to-host
+    alone, and both at once on two streams.  The concurrent time is the bound an
+    end-to-end step can reach with perfect overlap of copies and kernel."""
+    import torch
+    dsts = [torch.empty_like(t, device=dev) for t in tensors_h2d]
+    srcs = [torch.empty_like(t, device=dev) for t in tensors_d2h]
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def h2d(s):
+        with torch.cuda.stream(s):
+            for d, h in zip(dsts, tensors_h2d):
+                d.copy_(h, non_blocking=True)
+
+    def d2h(s):
+        with torch.cuda.stream(s):
+            for h, d in zip(tensors_d2h, srcs):
+                h.copy_(d, non_blocking=True)
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t0)
+        return best * 1e3
+
+    bi = sum(t.numel() * t.element_size() for t in tensors_h2d)
+    bo = sum(t.numel() * t.element_size() for t in tensors_d2h)
+    ms_in = timed(lambda: h2d(s1))
+    ms_out = timed(lambda: d2h(s2))
+    ms_both = timed(lambda: (h2d(s1), d2h(s2)))
+    return {"h2d_gbs": bi / (ms_in * 1e-3) / 1e9, "d2h_gbs": bo / (ms_out * 1e-3) / 1e9,
+            "h2d_ms": ms_in, "d2h_ms": ms_out, "both_ms": ms_both,
+            "link_gbs": (bi + bo) / (ms_both * 1e-3) / 1e9,
+            "how": "best of %d host-timed runs of one cudaMemcpyAsync per tensor, page-locked" % reps}
 
 
 def main():
@@ -242,6 +383,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None)
+    ap.add_argument("--no-small-workloads", action="store_true",
+                    help="skip the cold-L2 timings of the smaller workloads (per_config)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -441,6 +584,12 @@ def main():
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(e0.elapsed_time(e1) / args.e2e_steps, ws, dev)
     barrier()
+    link = link_bound(dev, [t for t in (hk, hg, hb, hcu) if t is not None], [hout])
+    del e2e_ws
+    default_line = (args.config == "B2_T16384_H32_K128" and wl.K == 128 and wl.chunk == 64
+                    and wl.k_dtype == "bf16" and out_dtype == "bf16")
+    per_config = (small_workload_lines(dev, stream, gdr, 50)
+                  if default_line and not args.no_small_workloads else None)
 
     if rank == 0:
         peak, peak_kind = measured_peaks()
@@ -467,11 +616,16 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                         "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                         "nominal_peak": NOMINAL_HBM_GBS,
                          "bytes_per_token_head": bpt},
             "e2e": {"value": aggregate_value(th_rank, e2e_ms, ws), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms,
-                    "call": "gdr_kkt_solve_host: page-locked host buffers, copies pipelined over two streams"},
+                    "call": "gdr_kkt_solve_host: page-locked host buffers, copies pipelined over two streams",
+                    "link": link, "link_gbs": link["link_gbs"],
+                    "of_link_bound": link["both_ms"] / e2e_ms},
+            "per_config": per_config,
             "gpu_launches": args.steps,
             "launch_stats": launch_stats,
             "clocks": clocks,

@@ -28,6 +28,7 @@ GDR_ERR_DEVICE = -6
 GDR_ERR_CUDA = -7
 GDR_ERR_TIMEOUT = -8
 GDR_ERR_SCRATCH = -9
+GDR_ERR_CU_SEQLENS = -10
 GDR_F32 = 0
 GDR_BF16 = 1
 GDR_F16 = 2
@@ -35,7 +36,8 @@ GDR_F16 = 2
 EXPORTED_SYMBOLS = ("gdr_kkt_solve", "gdr_kkt_solve_ex", "gdr_chunk_scaled_dot_kkt",
                     "gdr_solve_tril", "gdr_kkt_solve_unfused_noalloc", "gdr_kkt_solve_host",
                     "gdr_kkt_solve_host_workspace_bytes", "gdr_status_string",
-                    "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms", "gdr_selftest_bounded_wait")
+                    "gdr_kkt_solve_device_status", "gdr_kkt_solve_num_sms", "gdr_selftest_bounded_wait",
+                    "gdr_check_cu_seqlens")
 
 _lib = None
 _lock = threading.Lock()
@@ -87,6 +89,8 @@ def load_library():
             lib.gdr_kkt_solve_device_status.restype = ci
             lib.gdr_selftest_bounded_wait.argtypes = [vp]
             lib.gdr_selftest_bounded_wait.restype = ci
+            lib.gdr_check_cu_seqlens.argtypes = [vp, i64, i64, vp]
+            lib.gdr_check_cu_seqlens.restype = ci
             lib.gdr_kkt_solve_num_sms.argtypes = []
             lib.gdr_kkt_solve_num_sms.restype = ci
             _lib = lib
@@ -162,6 +166,29 @@ def kkt_solve_host_workspace_bytes(k_dtype: int, B: int, T: int, H: int, K: int,
     return int(n)
 
 
+def check_cu_seqlens_raw(cu_ptr: int, B: int, T: int, stream: int) -> int:
+    """Direct call of gdr_check_cu_seqlens (enqueues the device-side check of the
+    packed-sequence contract); returns the gdr_status code of the enqueue."""
+    return load_library().gdr_check_cu_seqlens(cu_ptr or None, B, T, stream or None)
+
+
+def check_cu_seqlens(cu_seqlens, T: int, stream=None) -> None:
+    """Enqueues the device-side check that cu_seqlens (int32 [B + 1] CUDA tensor)
+    starts at 0, never decreases and ends at most at T.  A broken array is
+    reported as GDR_ERR_CU_SEQLENS by the next device_status()."""
+    import torch
+
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda:
+        raise TypeError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    cu_seqlens = cu_seqlens.contiguous()
+    if stream is None:
+        stream = torch.cuda.current_stream(cu_seqlens.device).cuda_stream
+    with torch.cuda.device(cu_seqlens.device):
+        rc = check_cu_seqlens_raw(cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, int(T), int(stream))
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_check_cu_seqlens")
+
+
 def _gdr_dtype(dt, what: str) -> int:
     import torch
 
@@ -193,7 +220,7 @@ def num_sms() -> int:
 
 
 def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, output_dtype=None,
-              out=None, stream=None):
+              out=None, stream=None, validate_cu_seqlens: bool = False):
     """(I + A)^{-1} of every 64-token chunk and head, on the GPU.
 
     k: bf16 or fp16 [B, T, H, K] CUDA tensor, K in {64, 128, 192, 256}
@@ -202,7 +229,9 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
     ([1, T, H, K] with cu_seqlens); g: fp32 [B, T, H] or None; beta: fp32,
     bf16 or fp16 [B, T, H] or None; cu_seqlens: int32 [N + 1] CUDA tensor or
     None; output_dtype: torch.float32 (default), torch.bfloat16 or
-    torch.float16; chunk_size: 64 or 128.  Returns out [B, T, H, chunk_size]."""
+    torch.float16; chunk_size: 64 or 128.  validate_cu_seqlens=True first
+    enqueues the device-side check of the cu_seqlens contract (see
+    check_cu_seqlens).  Returns out [B, T, H, chunk_size]."""
     import torch
 
     if chunk_size not in (64, 128):
@@ -239,6 +268,8 @@ def kkt_solve(k, g=None, beta=None, cu_seqlens=None, chunk_size: int = 64, outpu
         raise ValueError("out has the wrong dtype, shape or layout")
     if stream is None:
         stream = torch.cuda.current_stream(k.device).cuda_stream
+    if validate_cu_seqlens and cu_seqlens is not None:
+        check_cu_seqlens(cu_seqlens, T, stream)
     with torch.cuda.device(k.device):
         rc = kkt_solve_ex_raw(k.data_ptr(), k_code, 0 if g is None else g.data_ptr(),
                               0 if beta is None else beta.data_ptr(), beta_code,
@@ -392,5 +423,6 @@ def solve_tril(A, cu_seqlens=None, chunk_size: int = 64, output_dtype=None, out=
 
 
 __all__ = ["kkt_solve", "chunk_scaled_dot_kkt", "solve_tril", "kkt_solve_raw", "kkt_solve_ex_raw",
-           "chunk_scaled_dot_kkt_raw", "solve_tril_raw", "kkt_solve_unfused_noalloc_raw", "device_status", "num_sms", "build", "load_library",
+           "chunk_scaled_dot_kkt_raw", "solve_tril_raw", "kkt_solve_unfused_noalloc_raw", "check_cu_seqlens",
+           "check_cu_seqlens_raw", "device_status", "num_sms", "build", "load_library",
            "status_string", "GdrError", "EXPORTED_SYMBOLS"]

@@ -1787,6 +1787,20 @@ __global__ void bounded_wait_probe_kernel(int *status) {
     }
 }
 
+// ------------------------------------------------------ cu_seqlens contract
+// Reads cu[0..B] and records GDR_ERR_CU_SEQLENS in the status word (unless an
+// earlier status is still unread) when cu[0] != 0, some cu[n] > cu[n+1], or
+// cu[B] > T.  Grid-stride over the B adjacent pairs; reads stay inside cu[0..B].
+__global__ void check_cu_seqlens_kernel(const int32_t *cu, int64_t B, int64_t T, int *status) {
+    bool bad = false;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < B; n += stride)
+        bad |= __ldg(cu + n) > __ldg(cu + n + 1);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        bad |= __ldg(cu) != 0 || static_cast<int64_t>(__ldg(cu + B)) > T;
+    if (bad) atomicCAS(status, static_cast<int>(GDR_OK), static_cast<int>(GDR_ERR_CU_SEQLENS));
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
@@ -1938,15 +1952,21 @@ const char *gdr_status_string(int status) {
     switch (status) {
         case GDR_OK: return "ok";
         case GDR_ERR_NULL: return "a required pointer is NULL";
-        case GDR_ERR_SHAPE: return "unsupported or inconsistent sizes (K in {64, 128, 192, 256}; B*T < 2^31)";
-        case GDR_ERR_CHUNK: return "chunk_size must be 64";
-        case GDR_ERR_DTYPE: return "unsupported dtype (k: bf16 or fp16; beta: fp32, bf16 or fp16; out: fp32, bf16 or fp16)";
+        case GDR_ERR_SHAPE:
+            return "unsupported or inconsistent sizes (K in {64, 128, 192, 256}; K <= 128 for fp32 keys and for "
+                   "chunk 128; B*T < 2^31)";
+        case GDR_ERR_CHUNK: return "chunk_size must be 64 (or 128 for the fused call, K <= 128)";
+        case GDR_ERR_DTYPE:
+            return "unsupported dtype (k: bf16 or fp16, or fp32 with K in {64, 128} in the fused chunk-64 call; "
+                   "beta: fp32, bf16 or fp16; out: fp32, bf16 or fp16)";
         case GDR_ERR_ALIGN: return "pointer misaligned (k and out 16 B, g 4 B, beta 2 B, cu_seqlens 4 B)";
         case GDR_ERR_DEVICE: return "no usable CUDA device (an sm_103 GPU is required)";
         case GDR_ERR_CUDA: return "a CUDA runtime or driver call failed";
         case GDR_ERR_TIMEOUT: return "a device-side pipeline wait timed out";
         case GDR_ERR_SCRATCH:
             return "problem too large for the allocation-free entry point (at most 262144 token-heads)";
+        case GDR_ERR_CU_SEQLENS:
+            return "cu_seqlens breaks its contract (cu[0] = 0, non-decreasing, cu[B] <= T)";
         default: return "unknown gdr_status";
     }
 }
@@ -2178,6 +2198,27 @@ int gdr_selftest_bounded_wait(void *stream) {
         return GDR_ERR_CUDA;
     }
     bounded_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status_ptr);
+    if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
+int gdr_check_cu_seqlens(const int32_t *cu_seqlens, int64_t B, int64_t T, void *stream) {
+    using namespace gdr;
+    if (!cu_seqlens) return GDR_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3) return GDR_ERR_ALIGN;
+    if (B < 0 || T < 0 || B >= (int64_t(1) << 31)) return GDR_ERR_SHAPE;
+    int sms = 0;
+    int rc = prepare_device(&sms);
+    if (rc != GDR_OK) return rc;
+    int *status_ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status_ptr), g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        return GDR_ERR_CUDA;
+    }
+    const int64_t blocks = (B + 255) / 256;
+    const int64_t cap = 4 * static_cast<int64_t>(sms);
+    const unsigned grid = static_cast<unsigned>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
+    check_cu_seqlens_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(cu_seqlens, B, T, status_ptr);
     if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }

@@ -44,14 +44,17 @@ extern "C" {
 typedef enum {
     GDR_OK = 0,
     GDR_ERR_NULL = -1,    /* a required pointer is NULL                        */
-    GDR_ERR_SHAPE = -2,   /* negative size, K not in {64,128,192,256}, overflow */
+    GDR_ERR_SHAPE = -2,   /* negative size, K not in {64,128,192,256} (K <= 128 for
+                             fp32 keys and for chunk 128), overflow           */
     GDR_ERR_CHUNK = -3,   /* chunk_size not 64 (or 128 for the fused call)      */
-    GDR_ERR_DTYPE = -4,   /* a dtype argument outside the supported set        */
+    GDR_ERR_DTYPE = -4,   /* a dtype argument outside the supported set (k: bf16
+                             or fp16, or fp32 in the fused chunk-64 call)      */
     GDR_ERR_ALIGN = -5,   /* a pointer is not aligned as documented below      */
     GDR_ERR_DEVICE = -6,  /* no current CUDA device, or it is not sm_103       */
     GDR_ERR_CUDA = -7,    /* a CUDA runtime/driver call failed (launch, TMA map) */
     GDR_ERR_TIMEOUT = -8, /* a device-side bounded wait ran out (see gdr_kkt_solve_device_status) */
-    GDR_ERR_SCRATCH = -9  /* too large for gdr_kkt_solve_unfused_noalloc's fixed scratch */
+    GDR_ERR_SCRATCH = -9, /* too large for gdr_kkt_solve_unfused_noalloc's fixed scratch */
+    GDR_ERR_CU_SEQLENS = -10 /* cu_seqlens breaks its contract (found by gdr_check_cu_seqlens) */
 } gdr_status;
 
 typedef enum {
@@ -76,8 +79,9 @@ typedef enum {
  *              cu[B] <= T.  Token rows outside every sequence are not written.
  *   B, T, H, K sizes; B, T or H equal to 0 is an empty problem (returns GDR_OK,
  *              enqueues nothing).  B*T must be below 2^31.
- *   chunk_size must be 64 (GDR_ERR_CHUNK otherwise, like the page's API, which
- *              raises ValueError for other chunk sizes).
+ *   chunk_size 64 (or 128, see gdr_kkt_solve_ex); any other value returns
+ *              GDR_ERR_CHUNK, as the page's API raises ValueError for chunk
+ *              sizes it does not support.
  *   out_dtype  GDR_F32, GDR_BF16 or GDR_F16.
  *   out        [B, T, H, 64] of out_dtype, 16-byte aligned.  Every row of a
  *              real token is fully written (zeros included); no separate
@@ -158,9 +162,12 @@ int gdr_solve_tril(const float *A, const int32_t *cu_seqlens, int64_t B, int64_t
  *
  *   Limit: at most 262144 token-heads per call (B*T*H, or T*H with
  *          cu_seqlens); larger problems return GDR_ERR_SCRATCH before anything
- *          is enqueued.  Other arguments and checks are those of
- *          gdr_kkt_solve_ex, and the result equals gdr_kkt_solve_ex's bit for
- *          bit.
+ *          is enqueued.
+ *   Inputs: those of the unfused chain, a subset of gdr_kkt_solve_ex's: keys
+ *          bf16 or fp16 only (fp32 keys return GDR_ERR_DTYPE) and chunk_size 64
+ *          only (128 returns GDR_ERR_CHUNK); K, beta and output types, layouts
+ *          and alignment as for gdr_kkt_solve_ex.  Where both accept the
+ *          arguments, the result equals gdr_kkt_solve_ex's bit for bit.
  *   Set-up: the first call on a device, with that device current, looks up the
  *          scratch's device address (cudaGetSymbolAddress) and keeps it for
  *          later calls; make that first call before any stream capture.
@@ -213,6 +220,25 @@ int gdr_kkt_solve_host(const void *k, int k_dtype, const float *g, const void *b
  * invalid types or sizes. */
 int64_t gdr_kkt_solve_host_workspace_bytes(int k_dtype, int64_t B, int64_t T, int64_t H, int64_t K,
                                            int chunk_size, int out_dtype);
+
+/*
+ * gdr_check_cu_seqlens - device-side check of the packed-sequence contract that
+ * gdr_kkt_solve and the other calls take on trust (no counterpart on the pages,
+ * which only show that varlen bookkeeping is where mistakes hide: MindSpeed-Ops
+ * PR #135 page, bot summary, the T_local fix).  The calls' tile schedule
+ * assumes cu[0] = 0, cu[n] <= cu[n+1] for every n < B, and cu[B] <= T; a
+ * broken array cannot make them write outside `out` or read outside the
+ * inputs, but chunks of the misdescribed sequences are then silently skipped.
+ * This call enqueues one small kernel on `stream` that reads cu_seqlens[0..B]
+ * (device memory, 4-byte aligned) and, when any of the three conditions fails,
+ * records GDR_ERR_CU_SEQLENS in the device status word (read and cleared by
+ * gdr_kkt_solve_device_status; an earlier unread status is kept).  It never
+ * traps and writes nothing else.  Opt-in: enqueue it before the call it guards,
+ * on the same stream.  Returns GDR_OK when enqueued (also for B = 0, which
+ * checks cu[0] only), GDR_ERR_NULL, GDR_ERR_ALIGN, GDR_ERR_SHAPE (B or T
+ * negative or B >= 2^31), GDR_ERR_DEVICE or GDR_ERR_CUDA.
+ */
+int gdr_check_cu_seqlens(const int32_t *cu_seqlens, int64_t B, int64_t T, void *stream);
 
 /* Human-readable text for a gdr_status value (static storage, never NULL). */
 const char *gdr_status_string(int status);

@@ -34,11 +34,36 @@ def test_library_builds_and_exports_every_declared_symbol():
     assert declared <= set(gdr.EXPORTED_SYMBOLS)
 
 
+def _header_status_codes():
+    text = open(os.path.join(ROOT, "include", "gdr_kkt_solve.h")).read()
+    body = re.search(r"typedef enum \{(.*?)\} gdr_status;", text, flags=re.S).group(1)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(GDR_[A-Z0-9_]+)\s*=\s*(-?\d+)", body)}
+
+
 def test_status_strings():
-    for code in range(-9, 1):
+    codes = _header_status_codes()
+    assert len(codes) == 11
+    for name, code in codes.items():
+        assert getattr(gdr, name) == code, name                 # binding constants = header enum
         s = gdr.status_string(code)
-        assert isinstance(s, str) and s and s != "unknown gdr_status"
+        assert isinstance(s, str) and s and s != "unknown gdr_status", name
+    assert gdr.status_string(min(codes.values()) - 1) == "unknown gdr_status"
     assert gdr.status_string(-99) == "unknown gdr_status"
+
+
+def test_status_strings_match_what_the_calls_accept():
+    # The texts state the accepted set as the header does: chunk 128 for the
+    # fused call, fp32 keys with K in {64, 128}, K <= 128 for those and chunk 128.
+    chunk = gdr.status_string(gdr.GDR_ERR_CHUNK)
+    assert "64" in chunk and "128" in chunk and "fused" in chunk
+    dtype = gdr.status_string(gdr.GDR_ERR_DTYPE)
+    assert "fp32" in dtype.split("beta")[0] and "{64, 128}" in dtype
+    for t in ("bf16", "fp16"):
+        assert t in dtype.split("beta")[0]
+    shape = gdr.status_string(gdr.GDR_ERR_SHAPE)
+    assert "{64, 128, 192, 256}" in shape and "K <= 128" in shape
+    assert "cu[0] = 0" in gdr.status_string(gdr.GDR_ERR_CU_SEQLENS)
+    assert "262144" in gdr.status_string(gdr.GDR_ERR_SCRATCH)
 
 
 # Fake, well-aligned addresses: validation must fail before anything uses them.
@@ -220,7 +245,9 @@ def _call_noalloc(**kw):
     (dict(cu=CU_PTR, B=3, T=70000, H=4), gdr.GDR_ERR_SCRATCH),
     (dict(chunk=32), gdr.GDR_ERR_CHUNK), (dict(out=0), gdr.GDR_ERR_NULL),
     (dict(out=OUT_PTR + 8), gdr.GDR_ERR_ALIGN), (dict(dtype=9), gdr.GDR_ERR_DTYPE),
-    (dict(K=100), gdr.GDR_ERR_SHAPE), (dict(T=0), gdr.GDR_OK), (dict(H=-1), gdr.GDR_ERR_SHAPE)])
+    (dict(K=100), gdr.GDR_ERR_SHAPE), (dict(T=0), gdr.GDR_OK), (dict(H=-1), gdr.GDR_ERR_SHAPE),
+    (dict(kd=gdr.GDR_F32), gdr.GDR_ERR_DTYPE), (dict(kd=gdr.GDR_F32, K=64), gdr.GDR_ERR_DTYPE),
+    (dict(chunk=128), gdr.GDR_ERR_CHUNK)])
 def test_noalloc_argument_checks_and_size_limit(kw, want):
     assert _call_noalloc(**kw) == want
 
@@ -289,3 +316,21 @@ def test_host_binding_rejects_device_tensors_and_bad_types():
         gdr.kkt_solve_host(k.float().double())                                       # fp64 keys
     with pytest.raises(ValueError):
         gdr.kkt_solve_host(k, out=torch.empty(1, 64, 2, 32))                          # wrong out shape
+
+
+@pytest.mark.parametrize("cu,B,T,want", [
+    (0, 3, 100, gdr.GDR_ERR_NULL), (CU_PTR + 2, 3, 100, gdr.GDR_ERR_ALIGN),
+    (CU_PTR, -1, 100, gdr.GDR_ERR_SHAPE), (CU_PTR, 3, -1, gdr.GDR_ERR_SHAPE),
+    (CU_PTR, 1 << 31, 100, gdr.GDR_ERR_SHAPE)])
+def test_check_cu_seqlens_argument_checks(cu, B, T, want):
+    assert gdr.check_cu_seqlens_raw(cu, B, T, 0) == want
+
+
+def test_check_cu_seqlens_valid_arguments_reach_the_device_check():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this test covers the no-device path")
+    assert gdr.check_cu_seqlens_raw(CU_PTR, 3, 100, 0) == gdr.GDR_ERR_DEVICE
+    assert gdr.check_cu_seqlens_raw(CU_PTR, 0, 0, 0) == gdr.GDR_ERR_DEVICE
+    with pytest.raises(TypeError):
+        gdr.check_cu_seqlens(torch.tensor([0, 5], dtype=torch.int32), 5)      # CPU tensor

@@ -3,10 +3,13 @@
 Tolerances (fixed for the method): fp32 output max_abs <= 2e-3 and
 mean_rel <= 1e-5; bf16 output max_abs <= 1.5e-2, with
 max_abs = max |gpu - ref| and mean_rel = sum |gpu - ref| / sum |ref| over the
-rows of real tokens.  Small workloads are compared element by element in full;
-the (2, 16384, 32, 128) workload is compared on a seeded sample of tiles
-(including every partial chunk) and checked on all rows for the properties that
-hold at any size.
+rows of real tokens.  bf16 output is held to two more bounds derived from its
+rounding: every element |gpu - ref| <= 2^-8 |ref| + 1e-3 (one bf16 rounding,
+2^-9 relative, plus the single tf32 pass of the merge), and mean_rel at most
+twice the mean_rel of rounding the exact result itself to bf16 (a systematic
+one-ulp error would be about four times it).  Every workload, the
+(2, 16384, 32, 128) one included, is compared with the oracle element by element
+on every row of a real token.
 """
 import numpy as np
 import pytest
@@ -45,6 +48,12 @@ def _metrics(got, ref):
     return float(d.max()), float(d.sum() / np.abs(ref).sum())
 
 
+def _rounding_mean_rel(ref):
+    """mean_rel of the exact result rounded to bf16 (round-to-nearest-even)."""
+    r = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    return float(np.abs(r - ref).sum() / np.abs(ref).sum())
+
+
 def _check(got, ref, out_dtype, what=""):
     max_abs, mean_rel = _metrics(got, ref)
     assert np.isfinite(got).all(), what
@@ -52,6 +61,11 @@ def _check(got, ref, out_dtype, what=""):
         assert max_abs <= F32_MAX_ABS and mean_rel <= F32_MEAN_REL, (what, max_abs, mean_rel)
     else:
         assert max_abs <= BF16_MAX_ABS, (what, max_abs, mean_rel)
+        excess = np.abs(got - ref) - (np.abs(ref) * 2.0 ** -8 + 1e-3)
+        assert excess.max() <= 0, (what, "element-wise bf16 bound", float(excess.max()))
+        rnd = _rounding_mean_rel(ref)
+        assert mean_rel <= 2.0 * rnd, (what, "bf16 mean_rel", mean_rel, rnd)
+    print(f"parity {what} {out_dtype}: max_abs={max_abs:.3e} mean_rel={mean_rel:.3e}")
     return max_abs, mean_rel
 
 
@@ -235,13 +249,14 @@ def test_golden_fixture_rows():
     _check(np.array(got), np.array(want), torch.float32, "golden")
 
 
-def test_full_size_bf16_sampled_parity_and_invariants():
+def test_full_size_bf16_every_tile():
+    # The benchmark's workload and launch: all 16384 (chunk, head) tiles against
+    # the oracle element by element, plus the exact structure of every row.
     dev = _dev()
     wl = workloads.CONFIGS["B2_T16384_H32_K128"]
     inp = workloads.make_inputs(wl)
     out = _run(inp, torch.bfloat16, dev)
     flat = out.view(-1, wl.H, 64)
-    # Properties on every row: finite, unit diagonal, zero strictly-upper part.
     assert torch.isfinite(flat).all()
     loc = torch.arange(wl.T, device=dev).remainder(64).repeat(wl.B)       # row within chunk
     cols = torch.arange(64, device=dev)
@@ -249,11 +264,13 @@ def test_full_size_bf16_sampled_parity_and_invariants():
     assert torch.all(diag == 1)
     upper = cols.view(1, 1, 64) > loc.view(-1, 1, 1)
     assert torch.all(flat.masked_select(upper) == 0)
-    # Sampled tiles against the oracle.
-    tiles = workloads.sample_tiles(wl, 256)
-    refs = oracle.kkt_solve_ref_tiles(inp["k"], inp["g"], inp["beta"], tiles)
-    got = np.concatenate([flat[r0:r0 + L, h].double().cpu().numpy() for (_, _, h, r0, L) in tiles])
-    _check(got, np.concatenate(refs), torch.bfloat16, "B2_T16384_H32_K128 sampled")
+    ref = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"])
+    got = out.double().cpu().numpy()
+    _check(got.reshape(-1, 64), ref.reshape(-1, 64), torch.bfloat16, "B2_T16384_H32_K128 all tiles")
+    # Per-tile view: the worst tile, so a fault confined to one CTA, pair slot or
+    # warpgroup would show even if the average stayed small.
+    per_tile = np.abs(got - ref).reshape(wl.B, wl.T // 64, 64, wl.H, 64).max(axis=(2, 4))
+    assert per_tile.max() <= BF16_MAX_ABS
 
 
 def _sampled_parity_and_invariants(wl, out_dtype, count):

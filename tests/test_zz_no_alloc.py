@@ -4,7 +4,9 @@ memory is planned up front, or code that cannot afford cudaMalloc's implicit
 device synchronisation).  It runs the unfused chain through the library's fixed
 device scratch, so it is compared, through the C ABI, with the existing entry
 point gdr_kkt_solve_ex on the same inputs, on two calls in a row of different
-sizes (the second call finds the first call's A in the shared scratch).
+sizes (the second call finds the first call's A in the shared scratch), and
+each result is also compared with the fp64 oracle directly, within the same
+tolerances as every other parity test.
 
 This file is named to be collected last, so that a run stopping at the first
 failure has already run every other test; it does not depend on them.
@@ -15,6 +17,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import gated_deltanet_chunked_gdr_gb300 as gdr  # noqa: E402
+import oracle  # noqa: E402
 import workloads  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -46,7 +49,17 @@ def _both(wl, out_dtype, dev, stream):
     assert gdr.device_status() == gdr.GDR_OK
     rows = np.arange(wl.token_heads // wl.H)
     ref, got = (o.reshape(-1, wl.H, 64)[torch.from_numpy(rows).to(dev)].double().cpu().numpy() for o in outs)
-    return ref, got
+    exact = oracle.kkt_solve_ref(inp["k"], inp["g"], inp["beta"], inp["cu_seqlens"]).reshape(-1, wl.H, 64)[rows]
+    return ref, got, exact
+
+
+def _within_tolerance(got, want, out_dtype, what):
+    assert np.isfinite(got).all(), what
+    d = np.abs(got - want)
+    if out_dtype == torch.float32:
+        assert d.max() <= F32_MAX_ABS and d.sum() / np.abs(want).sum() <= F32_MEAN_REL, (what, d.max())
+    else:
+        assert d.max() <= BF16_MAX_ABS, (what, d.max())
 
 
 def test_noalloc_matches_the_existing_entry_point_on_two_calls_in_a_row():
@@ -61,15 +74,11 @@ def test_noalloc_matches_the_existing_entry_point_on_two_calls_in_a_row():
     ]
     assert calls[0][0].token_heads <= 1 << 18
     for wl, out_dtype in calls:
-        ref, got = _both(wl, out_dtype, dev, stream)
-        assert np.isfinite(got).all()
-        d = np.abs(got - ref)
-        if out_dtype == torch.float32:
-            assert d.max() <= F32_MAX_ABS and d.sum() / np.abs(ref).sum() <= F32_MEAN_REL, wl.name
-        else:
-            assert d.max() <= BF16_MAX_ABS, wl.name
+        ref, got, exact = _both(wl, out_dtype, dev, stream)
+        _within_tolerance(got, ref, out_dtype, wl.name + " vs gdr_kkt_solve_ex")
+        _within_tolerance(got, exact, out_dtype, wl.name + " vs the oracle")
         # The chain runs the fused step's own arithmetic: the results agree exactly.
-        assert np.array_equal(got, ref), (wl.name, d.max())
+        assert np.array_equal(got, ref), (wl.name, np.abs(got - ref).max())
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
