@@ -203,6 +203,18 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
                  "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
+// Programmatic dependent launch: the grid may start while the previous grid on
+// the stream is still finishing (it is launched with programmatic stream
+// serialization).  Nothing may touch global memory before grid_dependency_wait
+// returns, which happens once every prerequisite grid has completed and its
+// writes are visible; grid_launch_dependents lets the next grid's CTAs begin
+// their own set-up as this grid's CTAs exit.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -825,6 +837,10 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = kUseTmem ? *tmem_slot : 0u;
+    // Set-up above touched only shared memory and TMEM: from here on global
+    // memory is read and written.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const int64_t n_local = (p.n_pairs > blockIdx.x)
                                 ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
@@ -1142,9 +1158,11 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                 if (lane == 0) mbar_arrive(bar_tempty + 8 * wg);
 
                 float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + a_row<kP>(i_e));
-                // Rows 0..31 only need columns j < 32 (A is strictly lower).  The
-                // kkt mode writes whole rows, zero at and above the diagonal.
-                const int n4 = (MODE == kModeKkt || (qd & 1)) ? 16 : 8;
+                // Row i of block I = i / 16 only needs columns j < 16 (I + 1): the
+                // blocks left of the diagonal and the diagonal block itself (A is
+                // strictly lower).  The kkt mode writes whole rows, zero at and
+                // above the diagonal.
+                const int n4 = MODE == kModeKkt ? 16 : 4 * ((i_e >> 4) + 1);
                 uint8_t *const sk = abuf + (tt_e ? kStage1Off : 0);
                 auto put = [&](int j4, float4 a) {
                     if constexpr (MODE == kModeKkt) {
@@ -1372,6 +1390,8 @@ __global__ void __launch_bounds__(kC128Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const int64_t n_local = (p.n_pairs > blockIdx.x)
                                 ? (p.n_pairs - 1 - blockIdx.x) / gridDim.x + 1
@@ -2101,16 +2121,32 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     prm.wg_ds = static_cast<uint32_t>((per_pair * grid * n_wg) / H);
     prm.wg_dh = static_cast<uint32_t>((per_pair * grid * n_wg) % H);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const unsigned gx = static_cast<unsigned>(grid);
+    // Programmatic stream serialization: the kernel may be scheduled while the
+    // stream's previous grid drains; it waits (griddepcontrol.wait) for that
+    // grid before touching global memory, so only its set-up overlaps.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err;
     if (CH == 128) {
-        kernel_c128_for(out_kind, static_cast<int>(K / 64))<<<gx, kC128Threads, kC128SmemBytes, st>>>(tmap, prm);
-        if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
-        return GDR_OK;
+        cfg.blockDim = dim3(kC128Threads);
+        cfg.dynamicSmemBytes = kC128SmemBytes;
+        err = cudaLaunchKernelEx(&cfg, kernel_c128_for(out_kind, static_cast<int>(K / 64)), tmap, prm);
+    } else {
+        const int nkb = static_cast<int>(in_dtype == GDR_F32 && kmode != kModeSolve ? K / 32 : K / 64);
+        cfg.blockDim = dim3(kmode == kModeF32Keys ? kNumThreadsF32Keys : kNumThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        err = cudaLaunchKernelEx(&cfg, kernel_for(kmode, out_kind, nkb), tmap, tmap_o, prm);
     }
-    const int nkb = static_cast<int>(in_dtype == GDR_F32 && kmode != kModeSolve ? K / 32 : K / 64);
-    kernel_for(kmode, out_kind, nkb)<<<gx, kmode == kModeF32Keys ? kNumThreadsF32Keys : kNumThreads,
-                                        kSmemBytes, st>>>(tmap, tmap_o, prm);
-    if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return GDR_ERR_CUDA;
+    }
     return GDR_OK;
 }
 
