@@ -80,7 +80,16 @@ constexpr int kAWGBytes = 36864;                    // >= kATile1Off + kATileByt
 constexpr int kStage1Off = 17408;                   // output staging of the second tile (1024-aligned)
 constexpr int kGWGBytes = 2 * 2 * 2 * kChunk * 4;   // g and v of two tiles, double buffered
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPrefetchPairs = 2;         // L2 prefetch distance of the key tiles, in pairs
+// L2 prefetch distance of the key tiles, in pairs: the producer's lanes 2 and
+// 3 issue cp.async.bulk.prefetch for pair q + d while lanes 0 and 1 load pair
+// q.  With d = 0 the prefetch goes out as soon as the producer reaches a pair,
+// ahead of its wait for a free stage; measured over d = -1 (none) .. 4 on
+// (2, 16384, 32, K), d = 0 is fastest where a pair's keys are one stage unit
+// (and for the chunk-128 kernel and the split fp32-key Gram) and d = 1 where
+// they are two 128-column units (K = 192, 256; fp32 keys as loaded, K = 128).
+__host__ __device__ constexpr int prefetch_pairs(int units_per_pair, bool split_f32) {
+    return units_per_pair == 2 && !split_f32 ? 1 : 0;
+}
 
 constexpr int kOffK = 0;
 constexpr int kOffA = kOffK + kNumStages * kStageBytes;
@@ -851,6 +860,7 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
     // of each of the pair's tiles; the Gram accumulates over a pair's units.
     constexpr int nkb = NKB;
     constexpr int nkc = kF32Keys ? nkb : (nkb + 1) >> 1;
+    constexpr int kPrefetchPairs = prefetch_pairs(nkc, kF32Keys);
     if (warp == kProducerWarp) {
         // Lanes 0 and 1 walk the two tiles of pair q (loaded into the stage ring),
         // lanes 2 and 3 those of pair q + kPrefetchPairs (prefetched into L2).
@@ -1398,6 +1408,7 @@ __global__ void __launch_bounds__(kC128Threads, 1)
                                 : 0;
     constexpr int nkb = NKB;
     constexpr int nkc = (nkb + 1) >> 1;
+    constexpr int kPrefetchPairs = 0;        // see prefetch_pairs
 
     if (warp == kC128Producer) {
         // As in the 64-token kernel; lane tt & 1 issues the copies of half tt.
