@@ -40,6 +40,7 @@ PAGE_FUSED_MS = {"B2_T16384_H32_K128": 4.9368}
 NOMINAL_HBM_GBS = 8000.0             # GB300 HBM3e nominal (~8 TB/s), for the second fraction
 L2_BYTES = 129 * 10**6               # GB300 L2 (two dies together)
 L2_FLUSH_BYTES = 512 << 20           # written before each step of a small workload
+SM_MAX_HZ = 2.07e9                   # GB300 maximum SM clock: turns a hold time into spin cycles
 
 
 ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4}
@@ -83,6 +84,15 @@ def recorded_traffic(wl, out_dtype: str):
     if not d or d.get("source_sha") != kernel_source_sha():
         return None
     return d.get("dram_bytes_per_launch")
+
+
+def hold_stream(stream, seconds: float) -> None:
+    """Hold `stream` with a delay kernel of about `seconds` (torch's spin kernel), so
+    that the launches queued behind it run back to back: the host's per-call latency
+    is then not part of a device-timed region, whose first event follows the hold."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(max(1, int(seconds * SM_MAX_HZ)))
 
 
 def reduce_max(x: float, ws: int, device=None) -> float:
@@ -306,6 +316,7 @@ def small_workload_lines(dev, stream, gdr, launches: int):
                 step()
                 b.record(stream)
             w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_stream(stream, 2e-3 + 1e-4 * launches)
             w0.record(stream)
             for _ in range(launches):
                 step()
@@ -435,8 +446,10 @@ def main():
         if ws > 1:
             torch.distributed.barrier()
 
+    t_enq = time.perf_counter()
     for _ in range(args.warmup):
         step()
+    enqueue_s = (time.perf_counter() - t_enq) / args.warmup     # host time per call
     torch.cuda.synchronize(dev)
     if gdr.device_status() != gdr.GDR_OK:
         raise RuntimeError("device status not ok after warm-up")
@@ -459,19 +472,31 @@ def main():
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)                                  # let the sampler start
-    ev0.record(stream)
-    if flush is None:
-        for _ in range(args.steps):
-            step()
-    else:
-        with torch.cuda.stream(stream):
-            for a, b in per_step:
-                flush.fill_(1.0)
-                a.record(stream)
+    # Back-to-back steps are queued behind a hold long enough for the host to
+    # enqueue all of them (checked: the region's first event must still be
+    # pending when the last step is queued, else the hold is lengthened and the
+    # region timed again).
+    hold_s, queued = 2e-3 + 4 * enqueue_s * args.steps, flush is not None
+    for _attempt in range(3):
+        if flush is None:
+            hold_stream(stream, hold_s)
+        ev0.record(stream)
+        if flush is None:
+            for _ in range(args.steps):
                 step()
-                b.record(stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+            queued = not ev0.query()
+        else:
+            with torch.cuda.stream(stream):
+                for a, b in per_step:
+                    flush.fill_(1.0)
+                    a.record(stream)
+                    step()
+                    b.record(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if queued:
+            break
+        hold_s *= 4
     barrier()
     clocks = sampler.stop()
     if flush is None:
@@ -488,6 +513,7 @@ def main():
         spread_n = min(args.steps, 500)
         per_launch = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                       for _ in range(spread_n)]
+        hold_stream(stream, 2e-3 + 4 * enqueue_s * spread_n)
         for a, b in per_launch:
             a.record(stream)
             step()
@@ -497,16 +523,20 @@ def main():
         per_launch = per_step
     us = sorted(a.elapsed_time(b) * 1e3 for a, b in per_launch)
     launch_stats = {"launches": len(us), "l2": "cold" if flush is not None else "not flushed (> 2 x L2)",
+                    "queued_behind_hold": bool(queued) if flush is None else None,
+                    "host_us_per_call": enqueue_s * 1e6,
                     "median_us": statistics.median(us),
                     "p10_us": us[int(0.1 * (len(us) - 1))], "p90_us": us[int(0.9 * (len(us) - 1))]}
     if flush is not None:
         w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_stream(stream, 2e-3 + 4 * enqueue_s * args.steps)
         w0.record(stream)
         for _ in range(args.steps):
             step()
         w1.record(stream)
         torch.cuda.synchronize(dev)
         launch_stats["warm_mean_us"] = w0.elapsed_time(w1) * 1e3 / args.steps
+    flushed = flush is not None
     del flush
     value = aggregate_value(th_rank, ms_step, ws)
     if gdr.device_status() != gdr.GDR_OK:
@@ -540,6 +570,7 @@ def main():
         torch.cuda.synchronize(dev)
         barrier()
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_stream(stream, 2e-3 + 4 * enqueue_s * chain_steps * len(fns))
         c0.record(stream)
         for _ in range(chain_steps):
             for f in fns:
@@ -611,6 +642,9 @@ def main():
                               if step_bytes >= 2 * L2_BYTES else
                               f"L2 flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write); "
                               "only the step is timed (events around each launch)"),
+                       "timing": ("CUDA events around the K launches, queued back to back behind a "
+                                  "delay kernel (host call latency not timed)" if not flushed else
+                                  "CUDA events around each launch"),
                        "parallelism": f"replicas x{ws} (independent tiles, no collective)",
                        "vs_baseline_ref": "Ascend 910B fused Triton time from the PR page table"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
