@@ -57,15 +57,6 @@ namespace gdr {
 
 constexpr int kChunk = 64;
 constexpr int kMaxHeadK = 256;                    // K = 64, 128, 192 or 256
-constexpr int kNumWG = 3;
-constexpr int kNumStages = 3;
-constexpr int kNumConsumerWarps = 4 * kNumWG;
-constexpr int kProducerWarp = kNumConsumerWarps;
-constexpr int kMmaWarp = kNumConsumerWarps + 1;
-constexpr int kNumThreads = (kNumConsumerWarps + 2) * 32;
-// The fp32-key instantiation adds two warps that split the key units.
-constexpr int kCvtWarp0 = kNumConsumerWarps + 2;
-constexpr int kNumThreadsF32Keys = kNumThreads + 64;
 
 constexpr int kBoxBytes = kChunk * 64 * 2;          // one (tile, K-half) box: 64 rows x 128 B
 constexpr int kStageBytes = 4 * kBoxBytes;          // [K-half][tile][64 rows][128 B] = 32 KB
@@ -92,16 +83,6 @@ __host__ __device__ constexpr int prefetch_pairs(int units_per_pair, bool split_
 }
 
 constexpr int kOffK = 0;
-constexpr int kOffA = kOffK + kNumStages * kStageBytes;
-constexpr int kOffG = kOffA + kNumWG * kAWGBytes;
-constexpr int kOffBar = kOffG + kNumWG * kGWGBytes;
-constexpr int kNumBars = 3 * kNumStages + 2 * kNumWG;   // full, empty, converted; tfull, tempty
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemUsed = kOffMisc + 64;
-constexpr int kSmemBytes = kSmemUsed + 1024;        // slack for 1024-byte alignment
-
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffA % 1024 == 0, "stages must keep 1024-byte alignment");
 
 constexpr uint64_t kWaitNs = 2000000000ull;         // 2 s bound for every wait
 constexpr uint32_t kSuspendNs = 1000000;             // a waiting thread sleeps until the phase completes (or 1 ms)
@@ -309,6 +290,7 @@ constexpr uint32_t idesc_f16_kind(bool bf16_keys) {
     return (1u << 4) | ((bf16_keys ? 1u : 0u) << 7) | ((bf16_keys ? 1u : 0u) << 10) |
            ((128u >> 3) << 17) | ((128u >> 4) << 24);
 }
+constexpr uint32_t kIdescBf16 = idesc_f16_kind(true);
 
 // ------------------------------------------------------------ tile schedule
 // Tile u = slot * H + h.  Fixed-length: slot = b * NT + c.  Varlen: sequence n
@@ -777,10 +759,12 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
 // fused result bit for bit.
 constexpr int kModeFused = 0, kModeKkt = 1, kModeSolve = 2;
 // The fused step with fp32 keys: the stage unit is one 32-column fp32 box per
-// tile (NKB = K / 32 units per pair); the MMA warp splits each unit into
-// big = x with the 13 low mantissa bits cleared (exact in tf32) and
-// small = x - big, and the Gram is big big^T + big small^T + small big^T on the
-// kind::tf32 tensor cores (the dropped small small^T is below 2^-20 relative).
+// tile (NKB = K / 32 units per pair); converter warps split each key x into
+// big = x rounded to tf32 and small = x - big (|small| <= 2^-11 |x|), and the
+// Gram is big big^T on the kind::tf32 tensor cores plus the cross products
+// bf16(big) bf16(small)^T + bf16(small) bf16(big)^T on the kind::f16 path.
+// Per product x_i x_j the bf16 roundings cost at most 2 * 2^-8 * 2^-11 and the
+// dropped small small^T at most 2^-22 of |x_i x_j|: about 2^-18 in all.
 constexpr int kModeF32Keys = 3;
 // The fused step with fp32 keys and bf16 output: the key units are the boxes of
 // fp32 columns as loaded, the MMA warp issues one kind::tf32 product per K step
@@ -789,6 +773,49 @@ constexpr int kModeF32Keys = 3;
 // within a fraction of one bf16 rounding of the output.
 constexpr int kModeF32KeysTf32 = 4;
 
+// Shared-memory plan and warp roles of the 64-token kernel, per mode.  Warps
+// 0 .. 4 NWG - 1 are the consumer warpgroups, then the producer warp, the MMA
+// warp and, for the split fp32-key Gram, the converter warps.  The split Gram
+// needs each unit's bf16 pair operand beside its keys, and its speed is set by
+// the key bytes in flight and by its converters (its consumers keep up with
+// two warpgroups), so it trades the third warpgroup's buffers and registers
+// for a six-unit ring of 16 KB key units, a three-unit ring of 16 KB pair
+// units and four converter warps; every other mode runs three consumer
+// warpgroups on a three-unit ring of 32 KB key units.
+template <int MODE>
+struct FusedLayout {
+    static constexpr bool kSplit = MODE == kModeF32Keys;
+    static constexpr int kNumWG = kSplit ? 2 : 3;
+    static constexpr int kNumStages = kSplit ? 6 : 3;                 // key units
+    static constexpr int kUnitBytes = kSplit ? 2 * kBoxBytes : kStageBytes;
+    static constexpr int kNumRem = kSplit ? 3 : 0;                    // bf16 pair units
+    static constexpr int kRemBytes = 2 * kBoxBytes;
+    static constexpr int kConsumerWarps = 4 * kNumWG;
+    static constexpr int kProducerWarp = kConsumerWarps;
+    static constexpr int kMmaWarp = kConsumerWarps + 1;
+    static constexpr int kCvtWarp0 = kConsumerWarps + 2;
+    // Converter warps: kCvtGroups groups of kCvtPerGroup warps; group g splits
+    // the key units v = g, g + kCvtGroups, ....  One group of four measured
+    // fastest: a converter warp shares its scheduler's issue slots with
+    // consumer warps, so a unit converts soonest spread over the most warps
+    // (two or three groups converting whole units in turn were much slower).
+    static constexpr int kCvtGroups = 1;
+    static constexpr int kCvtPerGroup = 4;
+    static constexpr int kCvtWarps = kSplit ? kCvtGroups * kCvtPerGroup : 0;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 2 + kCvtWarps);
+    static constexpr int kOffRem = kOffK + kNumStages * kUnitBytes;
+    static constexpr int kOffA = kOffRem + kNumRem * kRemBytes;
+    static constexpr int kOffG = kOffA + kNumWG * kAWGBytes;
+    static constexpr int kOffBar = kOffG + kNumWG * kGWGBytes;
+    // full, empty [stages]; tfull, tempty [warpgroups]; converted, pair unit free [pair units]
+    static constexpr int kNumBars = 2 * kNumStages + 2 * kNumWG + 2 * kNumRem;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 64 + 1024;           // slack for 1024-byte alignment
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kOffA % 1024 == 0 && kOffRem % 1024 == 0, "key units keep 1024-byte alignment");
+    static_assert(kThreads <= 512, "launch shape");
+};
+
 // OUT: kOutF32, kOutBF16 or kOutF16.  The merge runs split (fp32-accurate) for
 // fp32 and fp16 output and as one tf32 pass for bf16 output.  NKB = K / 64, the
 // 64-column key boxes per row; it only shapes the producer and MMA loops, which
@@ -796,11 +823,20 @@ constexpr int kModeF32KeysTf32 = 4;
 // solve mode the producer loads A tiles (two 32-column fp32 boxes per tile,
 // NKB = 2) and the MMA warp has nothing to do.
 template <int OUT, int NKB, int MODE>
-__global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 1)
+__global__ void __launch_bounds__(FusedLayout<MODE>::kThreads, 1)
     kkt_solve_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_out, const Params p) {
     static_assert(MODE != kModeKkt || OUT == kOutF32, "A is written as fp32");
     static_assert(MODE != kModeSolve || NKB == 2, "an A tile row is two 128-byte boxes");
+    using L = FusedLayout<MODE>;
+    constexpr int kNumWG = L::kNumWG;
+    constexpr int kNumStages = L::kNumStages;
+    constexpr int kNumRem = L::kNumRem;
+    constexpr int kRemMod = kNumRem > 0 ? kNumRem : 1;   // pair-unit ring modulus (unused without a split)
+    constexpr int kUnitBytes = L::kUnitBytes;
+    constexpr int kProducerWarp = L::kProducerWarp;
+    constexpr int kMmaWarp = L::kMmaWarp;
+    constexpr int kCvtWarp0 = L::kCvtWarp0;
     constexpr bool kUseTmem = MODE != kModeSolve;
     constexpr bool kF32Keys = MODE == kModeF32Keys;
     constexpr int kP = OUT == kOutBF16 ? 72 : 68;    // A buffer row layout (a_row)
@@ -811,14 +847,15 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + kOffBar;                       // [kNumStages]
+    const uint32_t bar_full = sbase + L::kOffBar;                    // [kNumStages]
     const uint32_t bar_empty = bar_full + 8 * kNumStages;            // [kNumStages]
     const uint32_t bar_tfull = bar_empty + 8 * kNumStages;           // [kNumWG]
     const uint32_t bar_tempty = bar_tfull + 8 * kNumWG;              // [kNumWG]
-    const uint32_t bar_cvt = bar_tempty + 8 * kNumWG;                // [kNumStages], fp32 keys
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
-    volatile int *wg_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);   // [kNumWG]
+    const uint32_t bar_cvt = bar_tempty + 8 * kNumWG;                // [kNumRem], split fp32 keys
+    const uint32_t bar_rfree = bar_cvt + 8 * kNumRem;                // [kNumRem], split fp32 keys
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
+    volatile int *wg_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 8);   // [kNumWG]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -834,7 +871,10 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
             mbar_init(bar_tfull + 8 * w, 1);
             mbar_init(bar_tempty + 8 * w, 4);
         }
-        for (int st = 0; st < kNumStages; ++st) mbar_init(bar_cvt + 8 * st, 2);
+        for (int u = 0; u < kNumRem; ++u) {
+            mbar_init(bar_cvt + 8 * u, L::kCvtPerGroup);
+            mbar_init(bar_rfree + 8 * u, 1);     // the MMA commit
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -901,7 +941,7 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                     const int box0 = kF32Keys ? kc : 2 * kc;
                     const int s = static_cast<int>(v % kNumStages);
                     const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
-                    const uint32_t st = sbase + kOffK + s * kStageBytes;
+                    const uint32_t st = sbase + kOffK + s * kUnitBytes;
                     int ok = 1;
                     if (lane == 0) {
                         ok = mbar_wait(bar_empty + 8 * s, ph ^ 1) ? 1 : 0;
@@ -933,45 +973,84 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
             }
         }
     } else if (kF32Keys && warp >= kCvtWarp0) {
-        // Converter warp c splits tile c's box of every unit in place: the tf32
-        // part (13 low mantissa bits cleared) stays, the remainder goes to the
-        // stage's second half; then it signals the unit's converted barrier.
-        const int c = warp - kCvtWarp0;
+        // The converter warps split every key unit v.  Each key x becomes
+        // big = x rounded to tf32 (split_tf32), written back in place for the
+        // kind::tf32 product big big^T, and small = x - big; bf16(big) and
+        // bf16(small) go to pair unit v % kNumRem (once the MMAs that read its
+        // previous contents have completed) as one 128-row operand whose
+        // 128-byte rows hold [bf16(big) of the unit's 32 columns | bf16(small)
+        // of them], for the cross products big small^T + small big^T on the
+        // kind::f16 path.  Then the warp signals the unit's converted barrier.
         const int64_t units = n_local * nkc;
-        for (int64_t v = 0; v < units; ++v) {
+        // Work items: (row r of the unit's 128, column octet o of 4), eight
+        // consecutive rows per warp instruction (conflict-free in the 128-byte
+        // swizzle).
+        constexpr int kItems = 128 * 4 / (32 * L::kCvtPerGroup);   // per lane
+        const int cg = (warp - kCvtWarp0) / L::kCvtPerGroup;       // converter group
+        const int t0 = ((warp - kCvtWarp0) % L::kCvtPerGroup) * 32 + lane;
+        for (int64_t v = cg; v < units; v += L::kCvtGroups) {
             if (*abort_flag) break;
             const int s = static_cast<int>(v % kNumStages);
             const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
+            const int u = static_cast<int>(v % kRemMod);
+            const uint32_t phr = static_cast<uint32_t>((v / kRemMod) & 1);
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(bar_full + 8 * s, ph) ? 1 : 0;
+            if (lane == 0)
+                ok = (mbar_wait(bar_full + 8 * s, ph) && mbar_wait(bar_rfree + 8 * u, phr ^ 1)) ? 1 : 0;
             if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
                 if (lane == 0) record_timeout(p, abort_flag);
                 break;
             }
-            float4 *const big = reinterpret_cast<float4 *>(smem + kOffK + s * kStageBytes + c * kBoxBytes);
-            float4 *const small = big + 2 * kBoxBytes / 16;
-#pragma unroll 4
-            for (int it = 0; it < kBoxBytes / 16 / 32; ++it) {
-                const int idx = lane + 32 * it;
-                const float4 x = big[idx];
-                float4 bg, m;
-                bg.x = __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
-                bg.y = __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
-                bg.z = __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
-                bg.w = __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
-                m.x = x.x - bg.x;
-                m.y = x.y - bg.y;
-                m.z = x.z - bg.z;
-                m.w = x.w - bg.w;
-                big[idx] = bg;
-                small[idx] = m;
+            uint8_t *const ku = smem + kOffK + s * kUnitBytes;
+            uint8_t *const pu = smem + L::kOffRem + u * L::kRemBytes;
+            // The lane's items go in batches whose loads are all issued before
+            // the batch's first store (the pair unit is not known not to alias
+            // the key unit, so a load left behind a store would wait for it).
+            constexpr int kBatch = kItems < 4 ? kItems : 4;
+#pragma unroll
+            for (int b0 = 0; b0 < kItems; b0 += kBatch) {
+                float4 xa[kBatch], xb[kBatch];
+#pragma unroll
+                for (int it = 0; it < kBatch; ++it) {
+                    const int item = t0 + 32 * L::kCvtPerGroup * (b0 + it);
+                    const int r = item >> 2, o = item & 3;
+                    xa[it] = *reinterpret_cast<const float4 *>(ku + r * 128 + (((2 * o) ^ (r & 7)) << 4));
+                    xb[it] = *reinterpret_cast<const float4 *>(ku + r * 128 + (((2 * o + 1) ^ (r & 7)) << 4));
+                }
+#pragma unroll
+                for (int it = 0; it < kBatch; ++it) {
+                    const int item = t0 + 32 * L::kCvtPerGroup * (b0 + it);
+                    const int r = item >> 2, o = item & 3;
+                    const float xv[8] = {xa[it].x, xa[it].y, xa[it].z, xa[it].w,
+                                         xb[it].x, xb[it].y, xb[it].z, xb[it].w};
+                    uint32_t bg[8], sm[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) split_tf32(xv[e], bg[e], sm[e]);
+                    *reinterpret_cast<uint4 *>(ku + r * 128 + (((2 * o) ^ (r & 7)) << 4)) =
+                        make_uint4(bg[0], bg[1], bg[2], bg[3]);
+                    *reinterpret_cast<uint4 *>(ku + r * 128 + (((2 * o + 1) ^ (r & 7)) << 4)) =
+                        make_uint4(bg[4], bg[5], bg[6], bg[7]);
+                    uint32_t pb[4], ps[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        pb[e] = pack16x2<kOutBF16>(__uint_as_float(bg[2 * e]), __uint_as_float(bg[2 * e + 1]));
+                        ps[e] = pack16x2<kOutBF16>(__uint_as_float(sm[2 * e]), __uint_as_float(sm[2 * e + 1]));
+                    }
+                    *reinterpret_cast<uint4 *>(pu + r * 128 + ((o ^ (r & 7)) << 4)) =
+                        make_uint4(pb[0], pb[1], pb[2], pb[3]);
+                    *reinterpret_cast<uint4 *>(pu + r * 128 + (((4 + o) ^ (r & 7)) << 4)) =
+                        make_uint4(ps[0], ps[1], ps[2], ps[3]);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_cvt + 8 * s);
+            if (lane == 0) mbar_arrive(bar_cvt + 8 * u);
         }
     } else if (kF32Keys && warp == kMmaWarp) {
-        // Lane 0 waits for the converted unit and issues the three tf32 products.
+        // Lane 0 waits for the converted unit and issues per K step of 8 the
+        // tf32 product big big^T, and per K step of 16 the two bf16 cross
+        // products from the pair unit (A and B descriptors 64 bytes apart in
+        // its rows); their completion frees both the key unit and the pair unit.
         if (lane == 0) {
             int64_t q = 0;
             bool failed = false;
@@ -983,24 +1062,30 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                 for (int kc = 0; kc < nkc; ++kc) {
                     const int64_t v = q * nkc + kc;
                     const int s = static_cast<int>(v % kNumStages);
-                    const uint32_t ph = static_cast<uint32_t>((v / kNumStages) & 1);
-                    if (!mbar_wait(bar_cvt + 8 * s, ph) ||
+                    const int u = static_cast<int>(v % kRemMod);
+                    const uint32_t phr = static_cast<uint32_t>((v / kRemMod) & 1);
+                    if (!mbar_wait(bar_cvt + 8 * u, phr) ||
                         (kc == 0 && !mbar_wait(bar_tempty + 8 * w, phw ^ 1))) {
                         record_timeout(p, abort_flag);
                         failed = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t st = sbase + kOffK + s * kStageBytes;
-                    const uint32_t sm = st + 2 * kBoxBytes;
+                    const uint32_t st = sbase + kOffK + s * kUnitBytes;
+                    const uint32_t sp = sbase + L::kOffRem + u * L::kRemBytes;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t db = smem_desc_sw128(st + ks * 32), dm = smem_desc_sw128(sm + ks * 32);
+                        const uint64_t db = smem_desc_sw128(st + ks * 32);
                         tc_mma_tf32(d, db, db, p.idesc, (kc | ks) ? 1u : 0u);
-                        tc_mma_tf32(d, db, dm, p.idesc, 1u);
-                        tc_mma_tf32(d, dm, db, p.idesc, 1u);
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const uint64_t pb = smem_desc_sw128(sp + ks * 32), ps = smem_desc_sw128(sp + 64 + ks * 32);
+                        tc_mma_f16(d, pb, ps, kIdescBf16, 1u);
+                        tc_mma_f16(d, ps, pb, kIdescBf16, 1u);
                     }
                     tc_commit(bar_empty + 8 * s);
+                    tc_commit(bar_rfree + 8 * u);
                     if (kc == nkc - 1) tc_commit(bar_tfull + 8 * w);
                 }
                 if (failed) break;
@@ -1035,7 +1120,7 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
                     tc_fence_after();
                     // One N = 128 product per K step: rows and columns both run over
                     // the pair's 128 key rows; each tile reads its own diagonal block.
-                    const uint32_t st = sbase + kOffK + s * kStageBytes;
+                    const uint32_t st = sbase + kOffK + s * kUnitBytes;
                     const int nb = (2 * kc + 1 < nkb) ? 2 : 1;
 #pragma unroll
                     for (int kh = 0; kh < nb; ++kh) {
@@ -1071,11 +1156,11 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
         const int i_e = 32 * (qd & 1) + lane;    // epilogue: row within the tile
         const int tid = threadIdx.x & 127;       // thread index inside the warpgroup
         const int g8 = lane >> 2, t4 = lane & 3; // mma.sync fragment coordinates
-        uint8_t *abuf = smem + kOffA + wg * kAWGBytes;
+        uint8_t *abuf = smem + L::kOffA + wg * kAWGBytes;
         float *const At0 = reinterpret_cast<float *>(abuf);
         float *const At1 = reinterpret_cast<float *>(abuf + kATile1Off);
         auto At = [At0, At1](int t) { return t ? At1 : At0; };
-        float *gbuf = reinterpret_cast<float *>(smem + kOffG + wg * kGWGBytes);   // [parity][tile][64]
+        float *gbuf = reinterpret_cast<float *>(smem + L::kOffG + wg * kGWGBytes);   // [parity][tile][64]
         float *vbuf = gbuf + 2 * 2 * kChunk;                                       // [parity][tile][64]
         const int bar_id = 1 + wg;
 
@@ -1136,7 +1221,8 @@ __global__ void __launch_bounds__(MODE == 3 ? kNumThreadsF32Keys : kNumThreads, 
             if constexpr (MODE == kModeSolve) {
                 // Every thread acquires the stage's completed phase itself.
                 if (!mbar_wait(bar_in, static_cast<uint32_t>(r & 1))) record_timeout(p, abort_flag);
-                const uint8_t *sa = smem + kOffK + wg * kStageBytes + tt_e * kBoxBytes + i_e * 128;
+                static_assert(MODE != kModeSolve || kNumStages == kNumWG, "stage wg holds pair q's A tiles");
+                const uint8_t *sa = smem + kOffK + wg * kUnitBytes + tt_e * kBoxBytes + i_e * 128;
                 float4 *Arow = reinterpret_cast<float4 *>(At(tt_e) + a_row<kP>(i_e));
                 const int n4 = (qd & 1) ? 16 : 8;
 #pragma unroll
@@ -1886,6 +1972,19 @@ KernelFn kernel_for(int mode, int out_kind, int nkb) {
     return kernel_for_nkb<kOutF32, kModeFused>(nkb);
 }
 
+// Launch shape of the 64-token kernel in a mode: threads per CTA, dynamic
+// shared memory and consumer warpgroups (the split fp32-key Gram has its own
+// layout; every other mode shares one).
+using SplitLayout = FusedLayout<kModeF32Keys>;
+using BaseLayout = FusedLayout<kModeFused>;
+static_assert(FusedLayout<kModeKkt>::kSmemBytes == BaseLayout::kSmemBytes &&
+                  FusedLayout<kModeSolve>::kSmemBytes == BaseLayout::kSmemBytes &&
+                  FusedLayout<kModeF32KeysTf32>::kSmemBytes == BaseLayout::kSmemBytes,
+              "one layout for every mode but the split Gram");
+int fused_threads(int mode) { return mode == kModeF32Keys ? SplitLayout::kThreads : BaseLayout::kThreads; }
+int fused_smem(int mode) { return mode == kModeF32Keys ? SplitLayout::kSmemBytes : BaseLayout::kSmemBytes; }
+int fused_wg(int mode) { return mode == kModeF32Keys ? SplitLayout::kNumWG : BaseLayout::kNumWG; }
+
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_ready[kMaxDevices];   // 0 unknown, 1 ready, -1 unsupported
 std::atomic<int> g_dev_sms[kMaxDevices];
@@ -1947,16 +2046,16 @@ int prepare_device(int *sms) {
                 for (int n = 1; n <= 4; ++n)
                     attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(m, o, n),
                                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                              kSmemBytes) == cudaSuccess;
+                                                              fused_smem(m)) == cudaSuccess;
         for (int o = 0; o < 3; ++o)
             for (int n = 2; n <= 4; n += 2)
                 attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(kModeF32Keys, o, n),
                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                          kSmemBytes) == cudaSuccess;
+                                                          fused_smem(kModeF32Keys)) == cudaSuccess;
         for (int n = 2; n <= 4; n += 2)
             attr_ok = attr_ok && cudaFuncSetAttribute(kernel_for(kModeF32KeysTf32, kOutBF16, n),
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                      kSmemBytes) == cudaSuccess;
+                                                      fused_smem(kModeF32KeysTf32)) == cudaSuccess;
         for (int o = 0; o < 3; ++o)
             for (int n = 1; n <= 2; ++n)
                 attr_ok = attr_ok && cudaFuncSetAttribute(kernel_c128_for(o, n),
@@ -2126,7 +2225,7 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     const int64_t grid = prm.n_pairs < sms ? prm.n_pairs : sms;
     // Tile strides of a CTA's and of a warpgroup's consecutive pairs.
     const int64_t per_pair = CH == 128 ? 1 : 2;
-    const int64_t n_wg = CH == 128 ? kC128WG : kNumWG;
+    const int64_t n_wg = CH == 128 ? kC128WG : fused_wg(kmode);
     prm.pair_ds = static_cast<uint32_t>((per_pair * grid) / H);
     prm.pair_dh = static_cast<uint32_t>((per_pair * grid) % H);
     prm.wg_ds = static_cast<uint32_t>((per_pair * grid * n_wg) / H);
@@ -2150,8 +2249,8 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
         err = cudaLaunchKernelEx(&cfg, kernel_c128_for(out_kind, static_cast<int>(K / 64)), tmap, prm);
     } else {
         const int nkb = static_cast<int>(in_dtype == GDR_F32 && kmode != kModeSolve ? K / 32 : K / 64);
-        cfg.blockDim = dim3(kmode == kModeF32Keys ? kNumThreadsF32Keys : kNumThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.blockDim = dim3(fused_threads(kmode));
+        cfg.dynamicSmemBytes = fused_smem(kmode);
         err = cudaLaunchKernelEx(&cfg, kernel_for(kmode, out_kind, nkb), tmap, tmap_o, prm);
     }
     if (err != cudaSuccess) {
