@@ -1436,7 +1436,32 @@ constexpr int kC128OffMisc = kC128OffBar + (2 * kC128Stages + 2 * kC128WG) * 8;
 constexpr int kC128SmemBytes = kC128OffMisc + 64 + 1024;
 constexpr uint32_t kC128TmemCols = 512;
 static_assert(kC128WGBytes % 16 == 0, "chunk-128 matrices");
+// 16-bit output of a full chunk leaves by four TMA stores of 64 x 64 boxes
+// (X11, the zero block, X21, X22), staged 128-byte swizzled at the first
+// 1024-byte boundary of the warpgroup's matrices: over M0 and most of M1 (read
+// into registers first), never over M2.
+__host__ __device__ constexpr int c128_stage_off(int wg) {
+    return (1024 - (kC128OffA + wg * kC128WGBytes) % 1024) % 1024;
+}
+static_assert(c128_stage_off(0) + 4 * 8192 <= kC128M2Off && c128_stage_off(1) + 4 * 8192 <= kC128M2Off &&
+                  c128_stage_off(2) + 4 * 8192 <= kC128M2Off,
+              "chunk-128 staging stays clear of M2");
 static_assert(kC128SmemBytes <= 232448, "chunk-128 shared memory budget");
+
+// Piece q (columns 8q .. 8q + 7) of row r of a lower-triangular 64 x 64 block
+// (fp32 rows kC128Pitch apart), above-diagonal values as zeros, packed to the
+// 16-bit output type.
+template <int OUT>
+__device__ __forceinline__ void c128_piece_lower(const float *M, int r, int q, uint32_t (&w)[4]) {
+    const float4 a = *reinterpret_cast<const float4 *>(M + r * kC128Pitch + 8 * q);
+    const float4 b = *reinterpret_cast<const float4 *>(M + r * kC128Pitch + 8 * q + 4);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float m[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m[e] = 8 * q + e <= r ? v[e] : 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = pack16x2<OUT>(m[2 * e], m[2 * e + 1]);
+}
 
 // The half tt (0 or 1) of a 128-token chunk as a 64-row tile.
 __device__ __forceinline__ Tile half_of(const Tile &c, int tt) {
@@ -1450,8 +1475,10 @@ __device__ __forceinline__ Tile half_of(const Tile &c, int tt) {
 
 template <int OUT, int NKB>
 __global__ void __launch_bounds__(kC128Threads, 1)
-    kkt_solve_c128_kernel(const __grid_constant__ CUtensorMap tmap_k, const Params p) {
+    kkt_solve_c128_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_out, const Params p) {
     constexpr bool SPLIT = OUT != kOutBF16;
+    constexpr bool kTmaOut = OUT != kOutF32;     // 16-bit output: full chunks by TMA store
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -1642,6 +1669,9 @@ __global__ void __launch_bounds__(kC128Threads, 1)
             }
             const RowIn rnext = load_row(p, nx, i);
 
+            // The previous chunk's TMA store has read its staging (over M0, M1)
+            // before the barrier below lets the epilogue write the matrices.
+            if (kTmaOut && tid == 0) bulk_wait_read();
             if (qd == 3 && lane == 0) {
                 int ok = mbar_wait(bar_tfull + 8 * wg, static_cast<uint32_t>(r & 1)) ? 1 : 0;
                 if (!ok) record_timeout(p, abort_flag);
@@ -1823,8 +1853,45 @@ __global__ void __launch_bounds__(kC128Threads, 1)
             named_bar_sync(bar_id, 128);                       // X complete
 
             // ---- store: every row of the chunk, 128 values; lower triangle of
-            //      X11 / X22 (masked), X21 in full, zeros elsewhere
-            {
+            //      X11 / X22 (masked), X21 in full, zeros elsewhere.  A full chunk
+            //      with 16-bit output goes out by TMA from the staging; otherwise
+            //      row by row.
+            if (kTmaOut && cur.L == 2 * kChunk) {
+                uint8_t *const stg = mb + c128_stage_off(wg);
+                // Item k of this thread: 16-byte piece q (8 values) of row r of a box.
+                uint32_t x11[4][4], x22[4][4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int idx = tid + 128 * k, r = idx >> 3, q = idx & 7;
+                    c128_piece_lower<OUT>(M0, r, q, x11[k]);
+                    c128_piece_lower<OUT>(M1, r, q, x22[k]);
+                }
+                named_bar_sync(bar_id, 128);                   // M0, M1 read: the staging may cover them
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int idx = tid + 128 * k, r = idx >> 3, q = idx & 7;
+                    const uint32_t off = stage_piece_off<true>(r, q);
+                    const float4 a = *reinterpret_cast<const float4 *>(M2 + r * kC128Pitch + 8 * q);
+                    const float4 b = *reinterpret_cast<const float4 *>(M2 + r * kC128Pitch + 8 * q + 4);
+                    *reinterpret_cast<uint4 *>(stg + off) = make_uint4(x11[k][0], x11[k][1], x11[k][2], x11[k][3]);
+                    *reinterpret_cast<uint4 *>(stg + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(stg + 16384 + off) =
+                        make_uint4(pack16x2<OUT>(a.x, a.y), pack16x2<OUT>(a.z, a.w), pack16x2<OUT>(b.x, b.y),
+                                   pack16x2<OUT>(b.z, b.w));
+                    *reinterpret_cast<uint4 *>(stg + 24576 + off) = make_uint4(x22[k][0], x22[k][1], x22[k][2], x22[k][3]);
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(bar_id, 128);                   // staging complete
+                if (tid == 0) {
+                    const uint32_t src = smem_u32(stg);
+                    const int row0 = static_cast<int>(cur.row0);
+                    tma_store_3d(&tmap_out, src, 0, cur.h, row0);
+                    tma_store_3d(&tmap_out, src + 8192, 64, cur.h, row0);
+                    tma_store_3d(&tmap_out, src + 16384, 0, cur.h, row0 + 64);
+                    tma_store_3d(&tmap_out, src + 24576, 64, cur.h, row0 + 64);
+                    bulk_commit();
+                }
+            } else {
                 char *const ob = reinterpret_cast<char *>(p.out);
                 constexpr int kEsz = OUT == kOutF32 ? 4 : 2;
                 constexpr int kRowsPerIt = OUT == kOutF32 ? 1 : 2;
@@ -1878,6 +1945,7 @@ __global__ void __launch_bounds__(kC128Threads, 1)
             cur = nx;
             rin = rnext;
         }
+        if (kTmaOut && tid == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -1934,7 +2002,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 using KernelFn = void (*)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap, Params);
-using KernelFn128 = void (*)(const __grid_constant__ CUtensorMap, Params);
+using KernelFn128 = void (*)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap, Params);
 
 template <int OUT, int MODE>
 KernelFn kernel_for_nkb(int nkb) {
@@ -2182,8 +2250,8 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
             return GDR_ERR_CUDA;
     }
     const int out_kind = mode == kModeKkt ? GDR_F32 : out_dtype;
-    CUtensorMap tmap_o;
-    if (chunk_size == kChunk) {     // the chunk-128 kernel stores rows without TMA
+    CUtensorMap tmap_o = {};
+    if (chunk_size == kChunk) {
         const int esz = out_kind == GDR_F32 ? 4 : 2;
         const CUtensorMapDataType odt = out_kind == GDR_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                         : out_kind == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -2191,6 +2259,18 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
         const cuuint64_t odims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(ntok)};
         const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(64 * esz), static_cast<cuuint64_t>(H * 64 * esz)};
         const cuuint32_t obox[3] = {static_cast<cuuint32_t>(128 / esz), 1, static_cast<cuuint32_t>(kChunk)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&tmap_o, odt, 3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GDR_ERR_CUDA;
+    } else if (out_kind != GDR_F32) {
+        // Chunk 128, 16-bit output: rows of 128 values, 64 x 64 boxes of 128-byte rows.
+        const CUtensorMapDataType odt = out_kind == GDR_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const cuuint64_t odims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(ntok)};
+        const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(128 * 2), static_cast<cuuint64_t>(H * 128 * 2)};
+        const cuuint32_t obox[3] = {64, 1, static_cast<cuuint32_t>(kChunk)};
         const cuuint32_t estr[3] = {1, 1, 1};
         if (encode(&tmap_o, odt, 3, out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -2246,7 +2326,7 @@ int launch(int mode, const void *in, int in_dtype, const float *g, const void *b
     if (CH == 128) {
         cfg.blockDim = dim3(kC128Threads);
         cfg.dynamicSmemBytes = kC128SmemBytes;
-        err = cudaLaunchKernelEx(&cfg, kernel_c128_for(out_kind, static_cast<int>(K / 64)), tmap, prm);
+        err = cudaLaunchKernelEx(&cfg, kernel_c128_for(out_kind, static_cast<int>(K / 64)), tmap, tmap_o, prm);
     } else {
         const int nkb = static_cast<int>(in_dtype == GDR_F32 && kmode != kModeSolve ? K / 32 : K / 64);
         cfg.blockDim = dim3(fused_threads(kmode));

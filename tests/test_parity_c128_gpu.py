@@ -98,3 +98,13 @@ def test_varlen():
     lens = (1, 128, 0, 129, 64, 65, 300, 2, 255)
     _parity(_wl("c128_varlen", len(lens), sum(lens), 3, seed=716, varlen_lengths=lens), "f32")
     _parity(workloads.CONFIGS["varlen8_H16_K128"].with_(chunk=C, name="c4_c128"), "f32")
+
+
+@pytest.mark.parametrize("out_name", ["bf16", "f16"])
+def test_varlen_16_bit_outputs(out_name):
+    # 16-bit output stores full chunks by TMA (four 64 x 64 boxes) and partial
+    # chunks row by row: full chunks here sit between partial ones, in packed
+    # sequences, so a box written past its chunk would show in a neighbour.
+    lens = (128, 1, 256, 127, 129, 0, 384, 65)
+    _parity(_wl("c128_varlen16", len(lens), sum(lens), 3, out=out_name, seed=717, varlen_lengths=lens),
+            out_name)
