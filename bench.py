@@ -86,6 +86,17 @@ def recorded_traffic(wl, out_dtype: str):
     return d.get("dram_bytes_per_launch")
 
 
+HOLD_LAUNCHES = 256                  # launches queued behind a hold (well inside the launch queue)
+HOLD_MAX_S = 0.5
+
+
+def hold_time(host_s_per_call: float, launches: int) -> float:
+    """A hold long enough for the host to queue min(launches, HOLD_LAUNCHES) calls
+    (four times the measured host time per call, plus 2 ms), at most HOLD_MAX_S.
+    Beyond those, the host keeps ahead of a GPU that runs them back to back."""
+    return min(HOLD_MAX_S, 2e-3 + 4 * host_s_per_call * min(launches, HOLD_LAUNCHES))
+
+
 def hold_stream(stream, seconds: float) -> None:
     """Hold `stream` with a delay kernel of about `seconds` (torch's spin kernel), so
     that the launches queued behind it run back to back: the host's per-call latency
@@ -446,10 +457,12 @@ def main():
         if ws > 1:
             torch.distributed.barrier()
 
-    t_enq = time.perf_counter()
+    t_enq = []
     for _ in range(args.warmup):
+        t0 = time.perf_counter()
         step()
-    enqueue_s = (time.perf_counter() - t_enq) / args.warmup     # host time per call
+        t_enq.append(time.perf_counter() - t0)
+    enqueue_s = statistics.median(t_enq)                       # host time per call
     torch.cuda.synchronize(dev)
     if gdr.device_status() != gdr.GDR_OK:
         raise RuntimeError("device status not ok after warm-up")
@@ -473,18 +486,19 @@ def main():
     sampler.start()
     time.sleep(0.3)                                  # let the sampler start
     # Back-to-back steps are queued behind a hold long enough for the host to
-    # enqueue all of them (checked: the region's first event must still be
-    # pending when the last step is queued, else the hold is lengthened and the
-    # region timed again).
-    hold_s, queued = 2e-3 + 4 * enqueue_s * args.steps, flush is not None
+    # enqueue the first HOLD_LAUNCHES of them (checked: the region's first event
+    # must still be pending by then, else the hold is lengthened and the region
+    # timed again); past those the host stays ahead of the GPU.
+    hold_s, queued = hold_time(enqueue_s, args.steps), flush is not None
     for _attempt in range(3):
         if flush is None:
             hold_stream(stream, hold_s)
         ev0.record(stream)
         if flush is None:
-            for _ in range(args.steps):
+            for n in range(args.steps):
                 step()
-            queued = not ev0.query()
+                if n + 1 == min(args.steps, HOLD_LAUNCHES):
+                    queued = not ev0.query()
         else:
             with torch.cuda.stream(stream):
                 for a, b in per_step:
@@ -496,7 +510,7 @@ def main():
         torch.cuda.synchronize(dev)
         if queued:
             break
-        hold_s *= 4
+        hold_s = min(HOLD_MAX_S, 4 * hold_s)
     barrier()
     clocks = sampler.stop()
     if flush is None:
@@ -513,7 +527,7 @@ def main():
         spread_n = min(args.steps, 500)
         per_launch = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                       for _ in range(spread_n)]
-        hold_stream(stream, 2e-3 + 4 * enqueue_s * spread_n)
+        hold_stream(stream, hold_time(3 * enqueue_s, spread_n))
         for a, b in per_launch:
             a.record(stream)
             step()
@@ -529,7 +543,7 @@ def main():
                     "p10_us": us[int(0.1 * (len(us) - 1))], "p90_us": us[int(0.9 * (len(us) - 1))]}
     if flush is not None:
         w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        hold_stream(stream, 2e-3 + 4 * enqueue_s * args.steps)
+        hold_stream(stream, hold_time(enqueue_s, args.steps))
         w0.record(stream)
         for _ in range(args.steps):
             step()
@@ -570,7 +584,7 @@ def main():
         torch.cuda.synchronize(dev)
         barrier()
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        hold_stream(stream, 2e-3 + 4 * enqueue_s * chain_steps * len(fns))
+        hold_stream(stream, hold_time(enqueue_s * len(fns), chain_steps))
         c0.record(stream)
         for _ in range(chain_steps):
             for f in fns:
