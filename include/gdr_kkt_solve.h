@@ -102,9 +102,10 @@ int gdr_kkt_solve(const void *k, const float *g, const void *beta,
  *   k_dtype    GDR_BF16 or GDR_F16 (the Gram runs on the tensor cores in that
  *              type; products are exact in the fp32 accumulator), or GDR_F32
  *              with K = 64 or 128 and chunk_size 64.  With fp32 or fp16 output
- *              each key is split into a tf32 part and a tf32 remainder and the
- *              Gram takes three tf32 products (about 2^-20 relative error);
- *              with bf16 output the Gram is one tf32 product of the keys as
+ *              each key is split into a tf32 part and a remainder and the Gram
+ *              is the tf32 product of the parts plus the two cross products
+ *              of their bf16 roundings (at most about 2^-18 relative error per
+ *              key product); with bf16 output the Gram is one tf32 product of the keys as
  *              given (each key element narrowed by at most 2^-10 of itself,
  *              below the output's own rounding).  fp32 keys with other K or
  *              chunk sizes return GDR_ERR_SHAPE or GDR_ERR_DTYPE.

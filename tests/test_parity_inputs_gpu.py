@@ -119,8 +119,9 @@ def test_fp16_all_inputs_fp16_output_large_k():
 @pytest.mark.parametrize("layout,out_name", [("fixed", "f32"), ("varlen", "f32"), ("fixed", "bf16")])
 def test_fp32_keys(K, layout, out_name):
     # fp32 keys: for fp32 (and fp16) output the Gram is formed from tf32 parts
-    # and remainders (three tf32 products), so fp32 output still meets the fp32
-    # tolerance; bf16 output takes one tf32 product (see below).
+    # and remainders (the tf32 product of the parts plus bf16 cross products,
+    # about 2^-18 relative per key product), so fp32 output still meets the
+    # fp32 tolerance; bf16 output takes one tf32 product (see below).
     if layout == "fixed":
         wl = workloads.Workload(f"f32keys_K{K}", 2, 300, 5, K, out_name, seed=800 + K, k_dtype="f32")
     else:
