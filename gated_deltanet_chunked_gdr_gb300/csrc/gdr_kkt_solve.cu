@@ -176,7 +176,11 @@ __device__ __noinline__ bool mbar_wait_limited(uint32_t bar, uint32_t parity) {
         if (global_timer() - t0 > LIMIT) return false;
     }
 }
+// The first (suspend-hinted) try_wait is inline, the bounded retry loop out of
+// line: most waits end in the first try_wait, and a call per wait measured
+// 1.9 % on (2, 16384, 32, 128) bf16.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_limited<kWaitNs>(bar, parity);
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
